@@ -1,0 +1,414 @@
+"""Benchmark of the co-batched layer step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload l8b]
+                    [--impl cf|reference] [--decode-sms N] [--sweep-decode-sms]
+
+Prints ONE JSON line (rank 0).  A step is one cf_layer_step over the
+workload's synthetic batch (all of: RMSNorm, fused QKV GEMM with RoPE and
+paged append, the decode || prefill attention fork, O-proj, RMSNorm, SwiGLU
+FFN).  `value` is stacked tokens per second (T rows per step) with inputs
+resident in HBM; `e2e` times the same step through host (pinned) buffers
+with the per-step host->device copies of x and of the batch metadata and the
+device->host copy of the output inside the timed region.  N > 1 runs N
+independent replicas (one per GPU, no collective in the data path) and
+reports the total over ranks divided by the slowest rank's time.
+
+--impl reference times the CPU fp64 oracle (the only reference arm: no other
+implementation of this method exists) on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "co-batched layer step µs & tokens/s; decode attn % HBM peak; GEMM % BF16 peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("CF_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value: float, device=None) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, value: float, device=None) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._thr = threading.Thread(target=self._read, daemon=True)
+            self._thr.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        import statistics
+        parsed = []
+        for t, line in self.rows:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                parsed.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [p for p in parsed if self.t0 and self.t1 and self.t0 <= p[0] <= self.t1]
+        use = inside if inside else parsed
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i, v in enumerate(p[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(p[1] for p in use), "sm_max_mhz": max(p[2] for p in use),
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# ------------------------------------------------------------------ work accounting
+def work_of(w, b):
+    """Algorithmic FLOPs / bytes of one step (what the roofline fractions use)."""
+    s = w.shape
+    T = b.n_tokens
+    H, d, Hq, Hkv, F = s.hidden, s.head_dim, s.n_q_heads, s.n_kv_heads, s.ffn_dim
+    gemm = {
+        "qkv": 2.0 * T * H * s.qkv_dim,
+        "oproj": 2.0 * T * Hq * d * H,
+        "gateup": 2.0 * T * H * 2 * F,
+        "down": 2.0 * T * F * H,
+    }
+    weights = {"qkv": 2.0 * s.qkv_dim * H, "oproj": 2.0 * H * Hq * d, "gateup": 4.0 * F * H, "down": 2.0 * H * F}
+    keys = sum(int(c) + 1 for c in b.dec_ctx)
+    dec_bytes = keys * Hkv * d * 2 * 2 + b.n_decode * Hq * d * 2 * 2
+    l, cp = b.prefill_len, b.prefill_prefix
+    pairs = l * cp + l * (l + 1) // 2
+    pre_flops = 4.0 * d * Hq * pairs
+    return {"gemm_flops": gemm, "weight_bytes": weights, "decode_bytes": float(dec_bytes),
+            "decode_keys": keys, "prefill_flops": pre_flops, "prefill_pairs": pairs}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(w, b, x, weights, kp, vp, rows):
+    import numpy as np
+    import oracle
+    W64 = oracle.LayerWeights64.from_torch({k: v.cpu() for k, v in weights.items()})
+    x64 = oracle.to_f64(x)
+    t0 = time.perf_counter()
+    oracle.layer_step(x64, W64, w.shape, b, kp, vp, rows=rows)
+    return time.perf_counter() - t0
+
+
+def reference_rows(b):
+    """Bounded sample for the CPU oracle: the first 64 chunk rows + all decodes."""
+    l = b.prefill_len
+    return list(range(min(64, l))) + list(range(l, l + b.n_decode))
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max((i.get("num_threads", 0) for i in info), default=os.cpu_count())
+    except Exception:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main arm
+def run_cf(args, rank, world, local, pg):
+    import numpy as np
+    import torch
+
+    import co_prefill_decode_gb300 as cf
+    import workload as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.workload]
+    b = wl.make_batch(w, args.seed)
+    x = wl.make_x(w, b, args.seed, "cuda")
+    W = wl.make_weights(w, args.seed, "cuda", unit_gains=True)
+    kp, vp = wl.make_pools(w, b, args.seed, "cuda")
+    T = b.n_tokens
+    eng = cf.Engine(cf.make_config(w.shape, T, max(b.n_decode, 1), args.decode_sms), W)
+    dec_ctx = torch.as_tensor(b.dec_ctx, device=dev)
+    dec_pages = torch.as_tensor(b.dec_pages, device=dev)
+    pre_pages = torch.as_tensor(b.pre_pages if len(b.pre_pages) else np.zeros(1, np.int32), device=dev)
+    batch = cf.batch_of(b.n_decode, dec_ctx, dec_pages, b.prefill_len, b.prefill_prefix, pre_pages)
+    pool = cf.pool_of(kp, vp)
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        eng.cf_layer_step(batch, x, out, pool, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, msg = eng.cf_get_error()
+    if st != 0:
+        raise RuntimeError(msg)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    eng.cf_set_profiling(True)
+    eng.cf_get_phase_times()   # reset
+    n_launch0 = eng.cf_launch_count()
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    clocks.mark("t1")
+    launches = eng.cf_launch_count() - n_launch0
+    phases, nsteps = eng.cf_get_phase_times()
+    eng.cf_set_profiling(False)
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(pg, ms_total, dev)
+    clocks.stop()
+
+    # e2e: host buffers, copies inside the timed region
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    meta_host = [t.cpu().pin_memory() for t in (dec_ctx, dec_pages, pre_pages)]
+    meta_dev = (dec_ctx, dec_pages, pre_pages)
+    h2d = x_host.numel() * 2 + sum(t.numel() * 4 for t in meta_host)
+    d2h = out_host.numel() * 2
+
+    def e2e_step():
+        x.copy_(x_host, non_blocking=True)
+        for hsrc, ddst in zip(meta_host, meta_dev):
+            ddst.copy_(hsrc, non_blocking=True)
+        eng.cf_layer_step(batch, x, out, pool, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ms_e2e = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    st, msg = eng.cf_get_error()
+    if st != 0:
+        raise RuntimeError(msg)
+
+    peaks = load_peaks()
+    wk = work_of(w, b)
+    per = {k: v / max(nsteps, 1) for k, v in phases.items()}   # ms per step
+    tok_total = sum_over_ranks(pg, float(T * args.steps), dev)
+    value = tok_total / (ms_total / 1e3)
+    ms_step = ms_total / args.steps
+    # per-kernel achieved rates (CUDA events around each phase inside the step)
+    kern = {}
+    for name, key in (("qkv", "qkv"), ("oproj", "oproj"), ("gateup", "gateup"), ("down", "down")):
+        t = per[key] / 1e3
+        kern[name] = {"ms": per[key], "tflops": wk["gemm_flops"][name] / t / 1e12 if t > 0 else None}
+    t_dec, t_pre = per["decode"] / 1e3, per["prefill"] / 1e3
+    kern["decode_attn"] = {"ms": per["decode"], "gbs": wk["decode_bytes"] / t_dec / 1e9 if t_dec > 0 else None,
+                           "sms": eng.cf_engine_decode_sms()}
+    kern["prefill_attn"] = {"ms": per["prefill"],
+                            "tflops": wk["prefill_flops"] / t_pre / 1e12 if t_pre > 0 else None}
+    kern["fork"] = {"ms": per["fork"], "serial_ms": per["decode"] + per["prefill"]}
+    kern["rmsnorm"] = {"ms": per["rmsnorm"] + per["rmsnorm2"]}
+    gemm_ms = sum(per[k] for k in ("qkv", "oproj", "gateup", "down"))
+    gemm_tflops = sum(wk["gemm_flops"].values()) / (gemm_ms / 1e3) / 1e12
+    peak_tc = peaks["bf16_tflops_sustained"]
+    dom = kern["gateup"]
+    roofline = {"kernel": "gate/up GEMM + SwiGLU epilogue", "bound": "tensor",
+                "achieved": dom["tflops"], "peak": peak_tc, "unit": "TFLOP/s",
+                "frac": dom["tflops"] / peak_tc if dom["tflops"] else None,
+                "traffic": None, "peak_source": peaks["source"] + " sustained bf16"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "layer_step_us": ms_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations and KV)",
+        "config": {"workload": f"{w.name}: {w.description}", "tokens_per_step": T, "n_decode": b.n_decode,
+                   "prefill_len": b.prefill_len, "prefill_prefix": b.prefill_prefix,
+                   "decode_keys": wk["decode_keys"], "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (weights + KV > 129 MB), no flush"},
+        "decode_attn_hbm_frac": (kern["decode_attn"]["gbs"] or 0) / peaks["hbm_gbs"],
+        "gemm_bf16_frac": gemm_tflops / peak_tc,
+        "gemm_tflops": gemm_tflops,
+        "fork_vs_serial": per["fork"] / max(1e-9, per["decode"] + per["prefill"]),
+        "kernels": kern,
+        "roofline": roofline,
+        "e2e": {"value": tok_total / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+        "peaks": peaks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rows = reference_rows(b)
+        secs = oracle_sample(w, b, x, W, kp, vp, rows)
+        line["cpu_baseline"] = {"value": len(rows) / secs, "unit": "tokens/s", "cores": blas_threads(),
+                                "kind": "oracle", "host_cores": os.cpu_count(),
+                                "sample": f"fp64 oracle layer step on {len(rows)} of {T} rows (first 64 chunk rows "
+                                          f"+ all decodes), {secs:.1f} s"}
+    if args.sweep_decode_sms:
+        line["decode_sms_sweep"] = sweep_decode_sms(eng, step, args, cf)
+    eng.close()
+    return line
+
+
+def sweep_decode_sms(eng, step, args, cf):
+    import torch
+    sms = cf.device_sm_count()
+    res = []
+    for frac in (0.10, 0.15, 0.20, 0.25, 0.30, 0.40, 0.50):
+        n = max(1, int(round(sms * frac)))
+        eng.cf_set_decode_sms(n)
+        for _ in range(3):
+            step()
+        eng.cf_set_profiling(True)
+        eng.cf_get_phase_times()
+        for _ in range(max(5, args.steps // 4)):
+            step()
+        ph, ns = eng.cf_get_phase_times()
+        eng.cf_set_profiling(False)
+        res.append({"decode_sms": n, "frac": frac, **{k: v / ns for k, v in ph.items()}})
+    eng.cf_set_decode_sms(0)
+    return res
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    import workload as wl
+    if rank != 0:
+        return None
+    w = wl.WORKLOADS[args.workload]
+    b = wl.make_batch(w, args.seed)
+    x = wl.make_x(w, b, args.seed)
+    W = wl.make_weights(w, args.seed, unit_gains=True)
+    kp, vp = wl.make_pools(w, b, args.seed)
+    rows = reference_rows(b)
+    for _ in range(args.warmup):
+        oracle_sample(w, b, x, W, kp, vp, rows[:8])
+    secs = [oracle_sample(w, b, x, W, kp, vp, rows) for _ in range(args.steps)]
+    total = sum(secs)
+    value = len(rows) * args.steps / total
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{w.name}: {w.description}", "rows_per_step": len(rows)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"fp64 oracle on {len(rows)} rows per step (first 64 chunk rows + "
+                                       f"all decodes)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="l8b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="cf", choices=["cf", "reference"])
+    ap.add_argument("--decode-sms", type=int, default=0)
+    ap.add_argument("--sweep-decode-sms", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local, pg = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_cf(args, rank, world, local, pg)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,255 @@
+"""Python binding of libcf, the GB300 co-batched layer-step library.
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+behind the C ABI declared in include/cf.h.  Tensors are passed as raw device
+pointers (``tensor.data_ptr()``) and streams as ``torch.cuda.Stream``
+handles; PyTorch only provides device memory and streams.  There is no CPU
+fallback: importing works without a GPU, but every call needs the built
+library (``python -m co_prefill_decode_gb300.build``) and a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcf.so")
+
+CF_OK, CF_ERR_INVALID_ARG, CF_ERR_UNSUPPORTED, CF_ERR_CUDA, CF_ERR_TIMEOUT, CF_ERR_OOM, CF_ERR_DEVICE = range(7)
+CF_EPI_NONE, CF_EPI_RESID_F32, CF_EPI_RESID_BF16, CF_EPI_SWIGLU = range(4)
+PHASES = ("rmsnorm", "qkv", "decode", "prefill", "fork", "oproj", "rmsnorm2", "gateup", "down", "step")
+
+# every symbol include/cf.h declares
+EXPORTS = (
+    "cf_device_sm_count", "cf_create", "cf_destroy", "cf_layer_step", "cf_decode_attn",
+    "cf_prefill_attn", "cf_gemm", "cf_kv_append", "cf_get_error", "cf_engine_buffer",
+    "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
+    "cf_launch_count", "cf_rmsnorm", "cf_qkv",
+)
+
+
+class CfError(RuntimeError):
+    def __init__(self, status: int, msg: str = ""):
+        super().__init__(f"libcf status {status}: {msg}")
+        self.status = status
+
+
+class cf_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int), ("page_size", ctypes.c_int),
+                ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float), ("qk_norm", ctypes.c_int),
+                ("max_tokens", ctypes.c_int), ("max_decode", ctypes.c_int), ("decode_sms", ctypes.c_int)]
+
+
+class cf_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_qkv", "w_o", "w_gate", "w_up", "w_down", "g_attn", "g_ffn", "g_q", "g_k")]
+
+
+class cf_kv_pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_pages", ctypes.c_int)]
+
+
+class cf_batch(ctypes.Structure):
+    _fields_ = [("n_decode", ctypes.c_int), ("dec_ctx", ctypes.c_void_p), ("dec_pages", ctypes.c_void_p),
+                ("dec_stride", ctypes.c_int), ("prefill_len", ctypes.c_int), ("prefill_prefix", ctypes.c_int),
+                ("pre_pages", ctypes.c_void_p)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libcf.so (fails loudly if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} not built: run python -m co_prefill_decode_gb300.build")
+    lib = ctypes.CDLL(path)
+    P, I, L, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+    sig = {
+        "cf_device_sm_count": (I, []),
+        "cf_create": (I, [ctypes.POINTER(cf_config), ctypes.POINTER(cf_weights), ctypes.POINTER(P)]),
+        "cf_destroy": (None, [P]),
+        "cf_layer_step": (I, [P, ctypes.POINTER(cf_batch), P, P, ctypes.POINTER(cf_kv_pool), P]),
+        "cf_decode_attn": (I, [P, P, L, ctypes.POINTER(cf_kv_pool), I, P, P, I, P, L, I, P]),
+        "cf_prefill_attn": (I, [P, P, ctypes.POINTER(cf_kv_pool), I, I, P, P, I, P]),
+        "cf_gemm": (I, [P, P, I, P, I, P, I, I, I, I, I, P, P]),
+        "cf_kv_append": (I, [P, P, P, I, P, ctypes.POINTER(cf_kv_pool), I, I, I, P]),
+        "cf_get_error": (I, [P, ctypes.c_char_p, I]),
+        "cf_engine_buffer": (P, [P, ctypes.c_char_p]),
+        "cf_engine_decode_sms": (I, [P]),
+        "cf_set_decode_sms": (I, [P, I]),
+        "cf_set_profiling": (I, [P, I]),
+        "cf_get_phase_times": (I, [P, ctypes.POINTER(F), I, ctypes.POINTER(I)]),
+        "cf_launch_count": (L, [P]),
+        "cf_rmsnorm": (I, [P, P, I, P, P, I, P]),
+        "cf_qkv": (I, [P, ctypes.POINTER(cf_batch), P, ctypes.POINTER(cf_kv_pool), P, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libcf takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libcf takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(lib, eng, status: int):
+    if status != CF_OK:
+        buf = ctypes.create_string_buffer(512)
+        if eng:
+            lib.cf_get_error(eng, buf, 512)
+        raise CfError(status, buf.value.decode(errors="replace"))
+
+
+def device_sm_count() -> int:
+    return int(load_library().cf_device_sm_count())
+
+
+def make_config(shape, max_tokens: int, max_decode: int, decode_sms: int = 0, page_size: int = 16) -> cf_config:
+    return cf_config(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn_dim, page_size,
+                     float(shape.rope_theta), float(shape.rms_eps), int(shape.qk_norm), max_tokens, max_decode,
+                     decode_sms)
+
+
+class Engine:
+    """Owns a cf_engine and keeps the weight tensors alive."""
+
+    def __init__(self, cfg: cf_config, weights: Dict[str, torch.Tensor]):
+        self.lib = load_library()
+        self.cfg = cfg
+        self._w = dict(weights)
+        w = cf_weights(*[_ptr(self._w.get(n)) for n in
+                         ("w_qkv", "w_o", "w_gate", "w_up", "w_down", "g_attn", "g_ffn", "g_q", "g_k")])
+        h = ctypes.c_void_p()
+        st = self.lib.cf_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h))
+        if st != CF_OK:
+            raise CfError(st, "cf_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.cf_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- C ABI wrappers (same names as the C entry points) ---------------------
+    def cf_layer_step(self, batch: cf_batch, x_in: torch.Tensor, x_out: torch.Tensor, pool: cf_kv_pool,
+                      stream=None):
+        _check(self.lib, self.handle, self.lib.cf_layer_step(self.handle, ctypes.byref(batch), _ptr(x_in),
+                                                             _ptr(x_out), ctypes.byref(pool), _stream(stream)))
+
+    def cf_decode_attn(self, q, q_row_stride: int, pool: cf_kv_pool, n: int, n_keys, pages, page_stride: int,
+                       out, out_row_stride: int, num_sms: int = 0, stream=None):
+        _check(self.lib, self.handle, self.lib.cf_decode_attn(
+            self.handle, _ptr(q), q_row_stride, ctypes.byref(pool), n, _ptr(n_keys), _ptr(pages), page_stride,
+            _ptr(out), out_row_stride, num_sms, _stream(stream)))
+
+    def cf_prefill_attn(self, q, pool: cf_kv_pool, l: int, prefix: int, pages, out, num_sms: int = 0,
+                        stream=None):
+        _check(self.lib, self.handle, self.lib.cf_prefill_attn(
+            self.handle, _ptr(q), ctypes.byref(pool), l, prefix, _ptr(pages), _ptr(out), num_sms,
+            _stream(stream)))
+
+    def cf_gemm(self, A, B, C, epilogue: int = CF_EPI_NONE, aux=None, stream=None):
+        M, K = A.shape
+        N = C.shape[1]
+        _check(self.lib, self.handle, self.lib.cf_gemm(
+            self.handle, _ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C), C.stride(0), M, N, K, epilogue,
+            _ptr(aux), _stream(stream)))
+
+    def cf_kv_append(self, k, v, slots, pool: cf_kv_pool, stream=None):
+        n, hkv, d = k.shape
+        _check(self.lib, self.handle, self.lib.cf_kv_append(
+            self.handle, _ptr(k), _ptr(v), n, _ptr(slots), ctypes.byref(pool), hkv, d, self.cfg.page_size,
+            _stream(stream)))
+
+    def cf_rmsnorm(self, x, gain, out, stream=None):
+        _check(self.lib, self.handle, self.lib.cf_rmsnorm(
+            self.handle, _ptr(x), int(x.dtype == torch.float32), _ptr(gain), _ptr(out), x.shape[0],
+            _stream(stream)))
+
+    def cf_qkv(self, batch: cf_batch, xn, pool: cf_kv_pool, q_out, stream=None):
+        _check(self.lib, self.handle, self.lib.cf_qkv(self.handle, ctypes.byref(batch), _ptr(xn),
+                                                      ctypes.byref(pool), _ptr(q_out), _stream(stream)))
+
+    def cf_get_error(self):
+        buf = ctypes.create_string_buffer(512)
+        st = self.lib.cf_get_error(self.handle, buf, 512)
+        return st, buf.value.decode(errors="replace")
+
+    def cf_engine_buffer(self, name: str) -> int:
+        return int(self.lib.cf_engine_buffer(self.handle, name.encode()) or 0)
+
+    def cf_engine_decode_sms(self) -> int:
+        return int(self.lib.cf_engine_decode_sms(self.handle))
+
+    def cf_set_decode_sms(self, n: int):
+        _check(self.lib, self.handle, self.lib.cf_set_decode_sms(self.handle, n))
+
+    def cf_set_profiling(self, on: bool):
+        _check(self.lib, self.handle, self.lib.cf_set_profiling(self.handle, int(on)))
+
+    def cf_get_phase_times(self):
+        ms = (ctypes.c_float * len(PHASES))()
+        steps = ctypes.c_int()
+        _check(self.lib, self.handle, self.lib.cf_get_phase_times(self.handle, ms, len(PHASES), ctypes.byref(steps)))
+        return dict(zip(PHASES, list(ms))), steps.value
+
+    def cf_launch_count(self) -> int:
+        return int(self.lib.cf_launch_count(self.handle))
+
+    # -- views of workspace tensors (read-only use in tests) ---------------------
+    def buffer(self, name: str, rows: int) -> torch.Tensor:
+        """A zero-copy torch view of a workspace tensor of the last step."""
+        c = self.cfg
+        width = {"xn": c.hidden, "q": c.n_q_heads * c.head_dim, "attn": c.n_q_heads * c.head_dim,
+                 "h": c.hidden, "hn": c.hidden, "act": c.ffn_dim}[name]
+        ptr = self.cf_engine_buffer(name)
+        if not ptr:
+            raise CfError(CF_ERR_INVALID_ARG, f"no buffer {name}")
+        if name == "h":
+            return torch.as_tensor(_DeviceArray(ptr, (rows, width), "<f4"), device="cuda")
+        return torch.as_tensor(_DeviceArray(ptr, (rows, width), "<i2"), device="cuda").view(torch.bfloat16)
+
+
+class _DeviceArray:
+    """__cuda_array_interface__ wrapper of a raw device pointer."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"data": (int(ptr), False), "shape": tuple(shape),
+                                         "typestr": typestr, "version": 3, "strides": None}
+
+
+def pool_of(k_pool: torch.Tensor, v_pool: torch.Tensor) -> cf_kv_pool:
+    return cf_kv_pool(_ptr(k_pool), _ptr(v_pool), int(k_pool.shape[0]))
+
+
+def batch_of(n_decode: int, dec_ctx, dec_pages, prefill_len: int, prefill_prefix: int, pre_pages) -> cf_batch:
+    stride = int(dec_pages.shape[1]) if dec_pages is not None and dec_pages.dim() == 2 else 1
+    return cf_batch(n_decode, _ptr(dec_ctx) if n_decode else None, _ptr(dec_pages) if n_decode else None, stride,
+                    prefill_len, prefill_prefix, _ptr(pre_pages) if prefill_len else None)

@@ -1,0 +1,395 @@
+// Dense GEMMs of the co-batched layer on the 5th-generation tensor cores.
+//
+// One persistent, warp-specialised kernel: warp 0 streams 128x64 A tiles and
+// BNx64 B tiles with TMA (128-byte swizzle) through an mbarrier ring; one
+// thread of warp 1 issues tcgen05.mma (M=128, N=BN, K=16, bf16 -> fp32 in
+// TMEM) and commits each stage back to the producer; warps 2-5 read the
+// accumulator from TMEM (double buffered, so the epilogue of tile i overlaps
+// the MMAs of tile i+1) and apply the fused epilogue.  The stacked
+// [prefill; decode] token matrix is the A operand, so every weight tile is
+// fetched once for both phases (ConfluxServe §4 "Cross-SP co-batch", App. B
+// Table 7: weight traffic amortised over all co-batched tokens).
+#include <stdio.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace cf {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+};
+
+CF_DEV uint8_t* align1024(uint8_t* p) {
+  uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+CF_DEV float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+CF_DEV void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
+    d[i] = w;
+  }
+}
+
+// QKV epilogue for one head of one row: columns [hcol, hcol + D) of this
+// thread's TMEM lane hold q, k or v of head `head` for stacked row `row`.
+template <int D>
+CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpilogue& e) {
+  const int Hq = e.Hq, Hkv = e.Hkv;
+  const int kind = head < Hq ? 0 : (head < Hq + Hkv ? 1 : 2);
+  __nv_bfloat16* dst = nullptr;
+  if (valid) {
+    if (kind == 0) {
+      dst = e.q_out + ((size_t)row * Hq + head) * D;
+    } else {
+      const int s = e.slot[row];
+      if (s >= 0) {
+        const int page = s / e.page_size, off = s % e.page_size;
+        const int kvh = kind == 1 ? head - Hq : head - Hq - Hkv;
+        __nv_bfloat16* pool = kind == 1 ? e.k_pool : e.v_pool;
+        dst = pool + (((size_t)page * Hkv + kvh) * e.page_size + off) * D;
+      }
+    }
+  }
+  float v[32], w[32];
+  if (kind == 2) {  // V: plain copy to the pool
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      tmem_ld32(taddr + c * 32, v);
+      tmem_ld_wait();
+      if (dst) store_bf16x32(dst + c * 32, v);
+    }
+    return;
+  }
+  float nrm = 1.0f;
+  const __nv_bfloat16* g = kind == 0 ? e.g_q : e.g_k;
+  if (e.qk_norm) {  // per-head RMSNorm over d (before RoPE)
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      tmem_ld32(taddr + c * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+    }
+    nrm = rsqrtf(ss / D + e.eps);
+  }
+  const float2* cs = e.rope_cs + (size_t)(valid ? row : 0) * (D / 2);
+  // rotate-half: element i pairs with i + D/2
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    tmem_ld32(taddr + c * 32, v);
+    tmem_ld32(taddr + D / 2 + c * 32, w);
+    tmem_ld_wait();
+    if (!dst) continue;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int i0 = c * 32 + i;
+      float x1 = v[i] * nrm, x2 = w[i] * nrm;
+      if (e.qk_norm) {
+        x1 *= bf16f(g[i0]);
+        x2 *= bf16f(g[i0 + D / 2]);
+      }
+      const float2 r = cs[i0];
+      v[i] = x1 * r.x - x2 * r.y;
+      w[i] = x1 * r.y + x2 * r.x;
+    }
+    store_bf16x32(dst + c * 32, v);
+    store_bf16x32(dst + D / 2 + c * 32, w);
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, GemmArgs p) {
+  using C = GemmCfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const WaitCtl wc{abort_flag, p.err, p.wait_ns};
+
+  const int num_m = (p.M + BM - 1) / BM;
+  const int num_n = EPI == EPI_SWIGLU ? p.N / (BN / 2) : p.N / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = p.K / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------- TMA producer
+      uint32_t stage = 0, phase = 0;
+      int issued_any = 0;
+      uint32_t last_phase[8];
+      for (int s = 0; s < 8; ++s) last_phase[s] = 0xffffffffu;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int mt = tile % num_m, nt = tile / num_m;
+        const int brow0 = EPI == EPI_SWIGLU ? nt * (BN / 2) : nt * BN;
+        const int brow1 = EPI == EPI_SWIGLU ? brow0 : brow0 + BN / 2;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
+          tma_load_2d(sb, &tmB0, &full[stage], kb * BK, brow0);
+          tma_load_2d(sb + C::B_BYTES / 2, &tmB1, &full[stage], kb * BK, brow1);
+          last_phase[stage] = phase;
+          issued_any = 1;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok && issued_any) {  // let our own copies land before the CTA exits
+        const WaitCtl drain_wc{abort_flag, nullptr, p.wait_ns};
+        volatile int dummy = 0;
+        const WaitCtl w2{&dummy, nullptr, p.wait_ns};
+        for (int s = 0; s < STAGES; ++s)
+          if (last_phase[s] != 0xffffffffu) mbar_wait(&full[s], last_phase[s], w2);
+        (void)drain_wc;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------- MMA issuer
+      constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+          }
+          issued = true;
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) umma_commit(&tfull[acc]);
+      }
+      if (!ok && issued) {  // wait for our MMAs before TMEM is released
+        volatile int dummy = 0;
+        const WaitCtl w2{&dummy, nullptr, p.wait_ns};
+        umma_commit(drain);
+        mbar_wait(drain, 0, w2);
+      }
+    }
+  } else {  // ---------------- epilogue warps 2..5
+    const int quarter = warp & 3;
+    const int r_in_tile = quarter * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
+      tc_fence_after();
+      const int mt = tile % num_m, nt = tile / num_m;
+      const int row = mt * BM + r_in_tile;
+      const bool valid = row < p.M;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      float v[32], w[32];
+      if constexpr (EPI == EPI_BF16) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          if (valid) store_bf16x32(out + c, v);
+        }
+      } else if constexpr (EPI == EPI_RESID_F32) {
+        float* out = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + nt * BN;
+        const __nv_bfloat16* res =
+            reinterpret_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * p.ld_aux + nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          if (valid) {
+            const uint4* r4 = reinterpret_cast<const uint4*>(res + c);
+            float4* o4 = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 q = r4[i];
+              o4[2 * i] = make_float4(v[8 * i + 0] + bf16lo(q.x), v[8 * i + 1] + bf16hi(q.x),
+                                      v[8 * i + 2] + bf16lo(q.y), v[8 * i + 3] + bf16hi(q.y));
+              o4[2 * i + 1] = make_float4(v[8 * i + 4] + bf16lo(q.z), v[8 * i + 5] + bf16hi(q.z),
+                                          v[8 * i + 6] + bf16lo(q.w), v[8 * i + 7] + bf16hi(q.w));
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_RESID_BF16) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * BN;
+        const float* res = reinterpret_cast<const float*>(p.aux) + (size_t)row * p.ld_aux + nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          if (valid) {
+            const float4* r4 = reinterpret_cast<const float4*>(res + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 q = r4[i];
+              v[4 * i] += q.x;
+              v[4 * i + 1] += q.y;
+              v[4 * i + 2] += q.z;
+              v[4 * i + 3] += q.w;
+            }
+            store_bf16x32(out + c, v);
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        __nv_bfloat16* out =
+            reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          tmem_ld32(taddr + c, v);
+          tmem_ld32(taddr + BN / 2 + c, w);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * w[i];
+            store_bf16x32(out + c, v);
+          }
+        }
+      } else if constexpr (EPI == EPI_QKV) {
+        const int D = p.qkv.head_dim;
+        const int col0 = nt * BN;
+        if (D == 128) {
+#pragma unroll 1
+          for (int hh = 0; hh < BN / 128; ++hh)
+            qkv_head<128>(taddr + hh * 128, row, valid, (col0 + hh * 128) / 128, p.qkv);
+        } else {
+#pragma unroll 1
+          for (int hh = 0; hh < BN / 64; ++hh)
+            qkv_head<64>(taddr + hh * 64, row, valid, (col0 + hh * 64) / 64, p.qkv);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+template <int BN, int EPI>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& p,
+                       int num_sms, cudaStream_t s) {
+  using C = GemmCfg<BN>;
+  auto k = gemm_kernel<BN, EPI>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int num_m = (p.M + BM - 1) / BM;
+  const int num_n = EPI == EPI_SWIGLU ? p.N / (BN / 2) : p.N / BN;
+  int grid = num_m * num_n;
+  int cap = p.max_ctas > 0 ? p.max_ctas : num_sms;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  k<<<grid, kThreads, C::SMEM, s>>>(a, b0, b1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_block_n(int epi) {
+  (void)epi;
+  return 256;
+}
+
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB0, const CUtensorMap& tmB1,
+                        const GemmArgs& a, int num_sms, cudaStream_t s) {
+  switch (a.epi) {
+    case EPI_BF16: return launch_one<256, EPI_BF16>(tmA, tmB0, tmB1, a, num_sms, s);
+    case EPI_RESID_F32: return launch_one<256, EPI_RESID_F32>(tmA, tmB0, tmB1, a, num_sms, s);
+    case EPI_RESID_BF16: return launch_one<256, EPI_RESID_BF16>(tmA, tmB0, tmB1, a, num_sms, s);
+    case EPI_SWIGLU: return launch_one<256, EPI_SWIGLU>(tmA, tmB0, tmB1, a, num_sms, s);
+    case EPI_QKV: return launch_one<256, EPI_QKV>(tmA, tmB0, tmB1, a, num_sms, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cf

@@ -1,0 +1,133 @@
+// Internal launch interfaces of libcf (not part of the C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cf {
+
+constexpr int kPageSize = 16;
+
+// ------------------------------------------------------------------ GEMM
+enum GemmEpi {
+  EPI_BF16 = 0,        // C bf16 = acc
+  EPI_RESID_F32 = 1,   // C fp32 = bf16 aux + acc
+  EPI_RESID_BF16 = 2,  // C bf16 = fp32 aux + acc
+  EPI_SWIGLU = 3,      // C bf16 = silu(acc[:, :BN/2]) * acc[:, BN/2:]
+  EPI_QKV = 4,         // QK-norm, RoPE, Q write, paged K/V append
+};
+
+struct QkvEpilogue {
+  int Hq, Hkv, head_dim, page_size, qk_norm, num_pages;
+  float eps;
+  const float2* rope_cs;          // [T][d/2] (cos, sin) at each row's position
+  const int* slot;                // [T] pool slot of each row (-1: skip)
+  const __nv_bfloat16* g_q;       // [d]
+  const __nv_bfloat16* g_k;       // [d]
+  __nv_bfloat16* q_out;           // [T][Hq][d]
+  __nv_bfloat16* k_pool;          // [pages][Hkv][ps][d]
+  __nv_bfloat16* v_pool;
+};
+
+struct GemmArgs {
+  int M, N, K;                    // N: output columns (SwiGLU: F)
+  int epi;
+  void* out;
+  long long ldo;                  // elements
+  const void* aux;                // residual
+  long long ld_aux;
+  QkvEpilogue qkv;
+  int* err;
+  unsigned long long wait_ns;
+  int max_ctas;                   // persistent grid cap (0 = all SMs)
+};
+
+// Builds a 2-D bf16 TMA descriptor with 128-byte swizzle: rows x cols
+// (cols contiguous, row stride `ld` elements), box = box_rows x 64.
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                  uint32_t box_rows, uint32_t box_cols);
+// 3-D: dims {d0 (contiguous), d1, d2}, strides in elements for d1, d2.
+bool make_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
+
+// A [M][K] (lda), B0/B1 halves of the weight tile: for plain GEMMs both
+// describe B [N][K]; for SwiGLU B0 = gate and B1 = up.
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB0, const CUtensorMap& tmB1,
+                        const GemmArgs& a, int num_sms, cudaStream_t s);
+int gemm_block_n(int epi);   // BN used for an epilogue kind
+
+// ------------------------------------------------------------------ row kernels
+struct PrepArgs {
+  // RMSNorm
+  const void* x;                  // [T][H] bf16 (in_f32 = 0) or fp32
+  int in_f32;
+  const __nv_bfloat16* gain;
+  float eps;
+  int T, H;
+  __nv_bfloat16* xn;              // [T][H]
+  // rope table + slots (skipped when rope_cs == nullptr)
+  float2* rope_cs;                // [T][d/2]
+  const double* inv_freq;         // [d/2]
+  int half_dim;
+  int* slot;                      // [T]
+  int l, prefix, n_decode;
+  const int* dec_ctx;
+  const int* dec_pages;
+  int dec_stride;
+  const int* pre_pages;
+  int num_pages, page_size;
+  int* err;
+};
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+
+cudaError_t launch_kv_append(const void* k, const void* v, int n, const int* slots, void* k_pool,
+                             void* v_pool, int num_pages, int Hkv, int d, int ps, int* err,
+                             cudaStream_t s);
+
+// ------------------------------------------------------------------ decode attention
+struct DecodeArgs {
+  const __nv_bfloat16* q;         // row j at q + j * q_stride, [Hq][d]
+  long long q_stride;
+  const __nv_bfloat16* k_pool;
+  const __nv_bfloat16* v_pool;
+  int num_pages;
+  int n;                          // requests
+  const int* n_keys;              // [n]; keys of request j = n_keys[j] + key_offset
+  int key_offset;
+  const int* pages;               // [n][page_stride]
+  int page_stride;
+  __nv_bfloat16* out;             // row j at out + j * out_stride, [Hq][d]
+  long long out_stride;
+  int Hq, Hkv, head_dim, page_size;
+  float scale_log2;               // log2(e) / sqrt(d)
+  float* part_o;                  // [max_items][G][d] fp32 (unnormalised)
+  float* part_ml;                 // [max_items][G][2] (max in log2 units, sum)
+  int* plan;                      // [n + 2]: chunk prefix sums, chunk pages
+  long long max_items;
+  int* err;
+};
+constexpr int kDecodeWarps = 8;
+long long decode_max_items(int max_decode, int Hkv, int max_ctas);
+cudaError_t launch_decode(const DecodeArgs& a, int num_ctas, cudaStream_t s);
+
+// ------------------------------------------------------------------ prefill attention
+struct PrefillArgs {
+  int l, prefix;                  // chunk length, cached prefix
+  int Hq, Hkv, head_dim, page_size, num_pages;
+  const int* pages;               // [ceil((prefix + l) / ps)]
+  __nv_bfloat16* out;             // row i at out + i * out_stride, [Hq][d]
+  long long out_stride;
+  float scale_log2;
+  int* counter;                   // work queue counter (zeroed before launch)
+  int* err;
+  unsigned long long wait_ns;
+};
+// tmQ: 3-D {d, Hq, rows} over q with box {64, 1, 128};
+// tmK/tmV: 2-D {d, pages*Hkv*ps} over the pools with box {64, 16}.
+cudaError_t launch_prefill(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const PrefillArgs& a, int num_ctas, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace cf

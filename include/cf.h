@@ -1,0 +1,234 @@
+/*
+ * cf.h — C ABI of libcf: one co-batched transformer layer step on one GB300.
+ *
+ * The method (ConfluxServe: Reconciling Resource Utilization and Parallelism
+ * Efficiency across Prefill and Decode in LLM Serving, §4 and Fig. 7): the
+ * tokens of a prefill chunk and the single tokens of many decode requests are
+ * stacked into one matrix [prefill rows; decode rows] so that every dense
+ * projection (fused QKV, O-proj, SwiGLU FFN) reads its weights once for both
+ * phases; attention then forks into decode attention over each request's own
+ * paged KV and causal chunked-prefill attention over the chunk's cached
+ * prefix, the two running concurrently on disjoint SM partitions (§6.1,
+ * "Coordinated attention overlap"), and the paths rejoin before O-proj.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensors are DEVICE memory owned by the caller; they must stay valid
+ *   until the work queued on the given stream has finished.  Weights must
+ *   outlive the engine.  The engine owns only its workspace.
+ * - bf16 means IEEE bfloat16 stored as uint16; row-major unless stated.
+ * - Paged KV pool (one for K, one for V): bf16 [num_pages][Hkv][page_size][d].
+ *   Each (page, kv head) is one contiguous page_size x d tile.  The slot of
+ *   token position p of a request with page table pt is
+ *   pt[p / page_size] * page_size + p % page_size (ConfluxServe §7: paged
+ *   blocks addressed through per-request block tables).
+ * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *   stream.  Every call is asynchronous on it.
+ * - Argument and shape checks are synchronous: a failing call returns a
+ *   status and launches nothing.  Problems only the device can see (a page id
+ *   outside the pool, a context longer than its page table, a bounded wait
+ *   that expired) set the engine's device error word; the kernels skip the
+ *   offending access instead of trapping.  cf_get_error() reports and clears
+ *   it.  No call traps or aborts.
+ * - An engine is not thread-safe.
+ */
+#ifndef CF_H
+#define CF_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CF_OK = 0,
+    CF_ERR_INVALID_ARG = 1,   /* bad pointer, size or shape; nothing launched   */
+    CF_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 96)    */
+    CF_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed               */
+    CF_ERR_TIMEOUT = 4,       /* a device-side bounded wait expired              */
+    CF_ERR_OOM = 5,           /* workspace allocation failed in cf_create        */
+    CF_ERR_DEVICE = 6         /* device error word set (bad page id, ...)        */
+} cf_status;
+
+/* Device error word bits (cf_get_error). */
+#define CF_DEVERR_PAGE     0x1   /* a page id outside [0, num_pages) was skipped */
+#define CF_DEVERR_CONTEXT  0x2   /* a context needs more pages than its table has */
+#define CF_DEVERR_TIMEOUT  0x4   /* a bounded mbarrier wait gave up              */
+
+typedef struct cf_engine cf_engine;
+
+/* Layer shape and engine limits. */
+typedef struct {
+    int hidden;          /* H                                                    */
+    int n_q_heads;       /* Hq                                                   */
+    int n_kv_heads;      /* Hkv; Hq % Hkv == 0, G = Hq / Hkv <= 16               */
+    int head_dim;        /* d: 64 or 128                                         */
+    int ffn_dim;         /* F (SwiGLU width); multiple of 128                    */
+    int page_size;       /* tokens per KV page: 16                               */
+    float rope_theta;    /* RoPE base                                            */
+    float rms_eps;       /* RMSNorm epsilon (also used by QK-norm)               */
+    int qk_norm;         /* 1: per-head RMSNorm of q and k over d before RoPE    */
+    int max_tokens;      /* largest T = l + n_decode of any step                 */
+    int max_decode;      /* largest n_decode of any step                         */
+    int decode_sms;      /* SMs given to decode attention in the fork; 0 = auto  */
+} cf_config;
+
+/* Weights, nn.Linear layout [out_features][in_features], bf16, device. */
+typedef struct {
+    const void* w_qkv;   /* [(Hq + 2 Hkv) d][H]: Q heads, then K heads, then V
+                            heads (Decode Token Parallelism §4.4, Eq. 1)         */
+    const void* w_o;     /* [H][Hq d]                                            */
+    const void* w_gate;  /* [F][H]                                               */
+    const void* w_up;    /* [F][H]                                               */
+    const void* w_down;  /* [H][F]                                               */
+    const void* g_attn;  /* [H] RMSNorm gain before QKV                          */
+    const void* g_ffn;   /* [H] RMSNorm gain before the FFN                      */
+    const void* g_q;     /* [d] QK-norm gain of q (NULL unless qk_norm)          */
+    const void* g_k;     /* [d] QK-norm gain of k (NULL unless qk_norm)          */
+} cf_weights;
+
+typedef struct {
+    void* k;             /* bf16 [num_pages][Hkv][page_size][d]                  */
+    void* v;             /* bf16 [num_pages][Hkv][page_size][d]                  */
+    int num_pages;
+} cf_kv_pool;
+
+/* One iteration's batch: a prefill chunk and n_decode resident decodes
+ * (ConfluxServe §6.2: chunk l_i with processed context c_i; decode requests
+ * with context c_i).  Rows of x are [l chunk rows; n_decode decode rows]. */
+typedef struct {
+    int n_decode;
+    const int* dec_ctx;    /* device int32 [n_decode]: c_j, tokens cached before
+                              this step; the new token sits at position c_j and
+                              attends to c_j + 1 keys                           */
+    const int* dec_pages;  /* device int32 [n_decode][dec_stride] page ids;
+                              needs ceil((c_j + 1) / page_size) valid entries   */
+    int dec_stride;
+    int prefill_len;       /* l, 0 = no chunk                                   */
+    int prefill_prefix;    /* c_p: chunk token i sits at position c_p + i       */
+    const int* pre_pages;  /* device int32 [ceil((c_p + l) / page_size)]       */
+} cf_batch;
+
+/* Largest number of SMs the device offers (0 if unknown).  No engine needed. */
+int cf_device_sm_count(void);
+
+/* Create an engine on the current device: checks the configuration, keeps
+ * the weight pointers, builds TMA descriptors and allocates the workspace
+ * (activations for max_tokens rows, split-K partials for max_decode
+ * requests), two streams' worth of events and the device error word.
+ * Returns CF_ERR_INVALID_ARG / CF_ERR_UNSUPPORTED for a bad configuration,
+ * CF_ERR_OOM if the workspace cannot be allocated. */
+cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out);
+
+/* Frees the workspace (synchronises the engine's streams first). NULL is ok. */
+void cf_destroy(cf_engine* e);
+
+/* One co-batched layer step (ConfluxServe Fig. 1, Fig. 7, §6.1):
+ *   xn = RMSNorm(x) g_attn; qkv = xn W_qkv^T; [QK-norm]; RoPE at each row's
+ *   position; K, V appended to the pool at slot(position) (Decode Token
+ *   Parallelism §4.3: rotary embeddings, append, attention);
+ *   fork: decode attention (rows l..T-1) on a second stream with decode_sms
+ *   SMs || causal prefill attention (rows 0..l-1) on `stream` with the rest;
+ *   join; h = x + O W_o^T (fp32); hn = RMSNorm(h) g_ffn;
+ *   x_out = h + (silu(hn W_gate^T) * (hn W_up^T)) W_down^T.
+ * x_in, x_out: bf16 [T][H], T = l + n_decode <= max_tokens; they must not
+ * overlap.  The pool is modified (T new K/V rows).  The cached slots that
+ * the step reads must not be written by other work in flight. */
+cf_status cf_layer_step(cf_engine* e, const cf_batch* b, const void* x_in, void* x_out,
+                        const cf_kv_pool* pool, void* stream);
+
+/* Split-K decode attention (ConfluxServe App. B, Table 7, "Decode
+ * Attention"; partial results merged with fp32 log-sum-exp as in Decode
+ * Token Parallelism §4.4, Eq. 4).  For request j and query head h:
+ *   out[j][h] = softmax(q[j][h] . K_j^T / sqrt(d)) V_j over the n_keys[j]
+ *   keys at positions 0..n_keys[j]-1 of the request, KV head h / G.
+ * q: bf16, row j at q + j * q_row_stride (elements), [Hq][d] inside the row.
+ * n_keys: device int32 [n] (>= 1).  pages: device int32 [n][page_stride].
+ * out: bf16, row j at out + j * out_row_stride, [Hq][d].
+ * num_sms: CTAs of the persistent grid (0 = all SMs).
+ * Uses the engine's workspace for the partials; n <= max_decode. */
+cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride,
+                         const cf_kv_pool* pool, int n, const int* n_keys,
+                         const int* pages, int page_stride, void* out,
+                         long long out_row_stride, int num_sms, void* stream);
+
+/* Causal chunked-prefill attention over a cached prefix (Adaptive Context
+ * Parallelism §2.1 mask M_ij = 0 iff j <= i; §2.2 Eq. 1 workload
+ * W(l, c_p) = l c_p + l(l+1)/2).  Chunk query i (position prefix + i) and
+ * head h attends to keys 0..prefix+i of the request, whose K/V (prefix and
+ * chunk) are already in the pool at the slots of `pages`.
+ * q: bf16 [l][Hq][d]; out: bf16 [l][Hq][d]; pages: device int32
+ * [ceil((prefix + l) / page_size)].  num_sms as above. */
+cf_status cf_prefill_attn(cf_engine* e, const void* q, const cf_kv_pool* pool, int l,
+                          int prefix, const int* pages, void* out, int num_sms,
+                          void* stream);
+
+/* RMSNorm of T rows of width H (the engine's hidden size): out = x /
+ * sqrt(mean(x^2) + eps) * gain, fp32 reduction (the pre-attention and
+ * pre-FFN norms of the layer; Decode Token Parallelism §4.3 "residual and
+ * normalization").  x: bf16 [T][H] (x_is_f32 = 0) or fp32 [T][H]; gain:
+ * bf16 [H]; out: bf16 [T][H]. */
+cf_status cf_rmsnorm(cf_engine* e, const void* x, int x_is_f32, const void* gain, void* out, int T,
+                     void* stream);
+
+/* The fused QKV stage of the layer on an already normalised input:
+ * qkv = xn W_qkv^T on the tensor cores; per head [QK-norm]; RoPE at each
+ * row's position (chunk row i: c_p + i; decode row j: c_j); q written to
+ * q_out (bf16 [T][Hq][d]); k and v appended to the pool at the slot of the
+ * row's position (Decode Token Parallelism §4.3: rotary embeddings, then the
+ * append).  xn: bf16 [T][H], T = l + n_decode <= max_tokens. */
+cf_status cf_qkv(cf_engine* e, const cf_batch* b, const void* xn, const cf_kv_pool* pool, void* q_out,
+                 void* stream);
+
+/* Epilogues of cf_gemm. */
+#define CF_EPI_NONE        0  /* C bf16 [M][N] = A B^T                               */
+#define CF_EPI_RESID_F32   1  /* C fp32 [M][N] = aux (bf16 [M][N]) + A B^T           */
+#define CF_EPI_RESID_BF16  2  /* C bf16 [M][N] = aux (fp32 [M][N]) + A B^T           */
+#define CF_EPI_SWIGLU      3  /* C bf16 [M][N] = silu(A B^T) * (A aux^T),
+                                 B = gate and aux = up, both bf16 [N][K]          */
+
+/* Dense GEMM on the tcgen05 tensor cores: A bf16 [M][K] (row stride lda
+ * elements), B bf16 [N][K] (row stride ldb), fp32 accumulation, epilogue
+ * as above (C row stride ldc elements; aux uses ldc for the residual
+ * epilogues and ldb for SwiGLU).  K % 64 == 0; N % 256 == 0 (N % 128 == 0
+ * for SwiGLU); all strides multiples of 8 and pointers 16-byte aligned.  The
+ * co-batched rows of A are independent: any row of C equals the same row
+ * computed alone (ConfluxServe §4: co-batching needs only a shared weight
+ * matrix and feature dimension). */
+cf_status cf_gemm(cf_engine* e, const void* A, int lda, const void* B, int ldb,
+                  void* C, int ldc, int M, int N, int K, int epilogue,
+                  const void* aux, void* stream);
+
+/* Paged KV append (ConfluxServe §4, Fig. 8: each request extends its own KV
+ * cache with its new tokens).  k, v: bf16 [n][Hkv][d]; slots: device int32
+ * [n] = page * page_size + offset.  Row r is copied bit for bit to
+ * pool.k[slot / ps][:, slot % ps, :] (and v).  Slots outside the pool are
+ * skipped and set CF_DEVERR_PAGE in the engine's error word (if e != NULL). */
+cf_status cf_kv_append(cf_engine* e, const void* k, const void* v, int n, const int* slots,
+                       const cf_kv_pool* pool, int n_kv_heads, int head_dim, int page_size,
+                       void* stream);
+
+/* Waits for the engine's streams, reads and clears the device error word.
+ * Returns CF_OK, CF_ERR_DEVICE or CF_ERR_TIMEOUT; writes a message to buf. */
+cf_status cf_get_error(cf_engine* e, char* buf, int len);
+
+/* Introspection for tests and benchmarks.
+ * cf_engine_buffer: device pointer of a workspace tensor of the last step:
+ *   "xn" bf16 [T][H], "q" bf16 [T][Hq][d], "attn" bf16 [T][Hq d],
+ *   "h" fp32 [T][H], "hn" bf16 [T][H], "act" bf16 [T][F]; NULL otherwise.
+ * cf_engine_decode_sms: SMs the fork gives decode attention for n_sms total.
+ * cf_set_profiling: 1 = record CUDA events around every phase of each step.
+ * cf_get_phase_times: accumulated milliseconds per phase since the last
+ *   reset (order: rmsnorm, qkv, decode, prefill, fork, oproj, rmsnorm2,
+ *   gateup, down, step) and the number of steps; resets the counters.
+ * cf_launch_count: kernels this engine launched since creation. */
+void* cf_engine_buffer(cf_engine* e, const char* name);
+int cf_engine_decode_sms(cf_engine* e);
+cf_status cf_set_decode_sms(cf_engine* e, int n);
+cf_status cf_set_profiling(cf_engine* e, int on);
+cf_status cf_get_phase_times(cf_engine* e, float* ms, int n, int* steps);
+long long cf_launch_count(cf_engine* e);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CF_H */

@@ -315,4 +315,7 @@ def layer_step(x: np.ndarray, W: LayerWeights64, shape, batch, k_pool, v_pool,
         "rows": rows, "out": out, "h": h, "hn": hn, "act": act,
         "attn": attn[where], "q": q[where], "k": k[where], "v": v[where],
         "xn": xn[where], "slots": np.asarray(slots, dtype=np.int64),
+        # every row whose q/k/v were computed (all chunk rows up to the last
+        # selected one, then the selected decode rows), in stacked-row order
+        "need_rows": need, "q_need": q, "k_need": k, "v_need": v, "xn_need": xn,
     }

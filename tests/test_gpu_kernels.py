@@ -1,0 +1,249 @@
+"""GPU parity of the individual C-ABI kernels against the fp64 oracle / exact
+references (cf_gemm, cf_kv_append, cf_decode_attn, cf_prefill_attn)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workload as wl
+from helpers import assert_close, f64, fill_positions, randn_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cf():
+    import co_prefill_decode_gb300 as cf
+    cf.load_library()
+    return cf
+
+
+def engine_for(cf, shape, max_tokens=4096, max_decode=256):
+    W = {k: v.cuda() for k, v in wl.make_weights(wl.Workload("t", shape, 1, (1,), 0, 0), 7).items()}
+    return cf.Engine(cf.make_config(shape, max_tokens, max_decode), W)
+
+
+def int_bf16(shape, seed, lo=-4, hi=4):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, shape, generator=g).to(torch.bfloat16).cuda()
+
+
+# --------------------------------------------------------------------- GEMM
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (68, 512, 256), (200, 768, 4096), (1040, 512, 1024),
+                                   (300, 256, 8192), (1040, 6144, 512), (4128, 2048, 256)])
+def test_gemm_exact_integers(cf, M, N, K):
+    """Small integers: fp32 accumulation is exact, so the GPU equals the integer
+    product bit for bit (fp32 out via the residual epilogue with zero aux) and
+    its bf16 rounding (plain epilogue)."""
+    eng = engine_for(cf, wl.TINY)
+    A, B = int_bf16((M, K), 1), int_bf16((N, K), 2)
+    exact = f64(A) @ f64(B).T
+    C32 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    eng.cf_gemm(A, B, C32, cf.CF_EPI_RESID_F32, aux=torch.zeros(M, N, dtype=torch.bfloat16, device="cuda"))
+    C16 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(A, B, C16, cf.CF_EPI_NONE)
+    torch.cuda.synchronize()
+    assert np.array_equal(f64(C32), exact)
+    assert np.array_equal(f64(C16), oracle.bf16_round(exact))
+
+
+def test_gemm_epilogues(cf):
+    eng = engine_for(cf, wl.TINY)
+    M, N, K = 333, 512, 1024
+    A, B = randn_bf16((M, K), 3), randn_bf16((N, K), 4, std=0.03)
+    U = randn_bf16((N, K), 5, std=0.03)
+    res16 = randn_bf16((M, N), 6)
+    res32 = torch.randn(M, N, generator=torch.Generator().manual_seed(7)).cuda()
+    a, b, u = f64(A), f64(B), f64(U)
+    out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    eng.cf_gemm(A, B, out, cf.CF_EPI_RESID_F32, aux=res16)
+    o2 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(A, B, o2, cf.CF_EPI_RESID_BF16, aux=res32)
+    o3 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(A, B, o3, cf.CF_EPI_SWIGLU, aux=U)
+    torch.cuda.synchronize()
+    assert_close(out, f64(res16) + a @ b.T, "resid f32", 1e-5, 1e-6)
+    assert_close(o2, oracle.bf16_round(f64(res32) + a @ b.T), "resid bf16")
+    assert_close(o3, oracle.bf16_round(oracle.swiglu(a @ b.T, a @ u.T)), "swiglu")
+
+
+def test_gemm_swiglu_many_tiles(cf):
+    """More tiles than CTAs: each CTA walks several tiles through both TMEM
+    accumulator buffers."""
+    eng = engine_for(cf, wl.TINY)
+    M, F, K = 300, 14336, 512
+    A, G, U = int_bf16((M, K), 21, -2, 2), int_bf16((F, K), 22, -1, 1), int_bf16((F, K), 23, -1, 1)
+    out = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(A, G, out, cf.CF_EPI_SWIGLU, aux=U)
+    torch.cuda.synchronize()
+    a = f64(A)
+    ref = oracle.bf16_round(oracle.swiglu(a @ f64(G).T, a @ f64(U).T))
+    assert_close(out, ref, "swiglu many tiles", 8e-3, 1e-4)
+
+
+def test_gemm_rows_are_independent(cf):
+    """Co-batching invariance (ConfluxServe §4): a row of the stacked GEMM is
+    bit-identical to the same row computed in a smaller batch."""
+    eng = engine_for(cf, wl.TINY)
+    K, N = 2048, 768
+    A, B = randn_bf16((700, K), 8), randn_bf16((N, K), 9, std=0.02)
+    full = torch.empty(700, N, dtype=torch.bfloat16, device="cuda")
+    part = torch.empty(130, N, dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(A, B, full)
+    eng.cf_gemm(A[500:630].contiguous(), B, part)
+    torch.cuda.synchronize()
+    assert torch.equal(full[500:630], part)
+
+
+def test_gemm_rejects_bad_shapes(cf):
+    eng = engine_for(cf, wl.TINY)
+    A, B = randn_bf16((64, 100), 1), randn_bf16((256, 100), 2)
+    C = torch.empty(64, 256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cf.CfError) as e:
+        eng.cf_gemm(A, B, C)
+    assert e.value.status == cf.CF_ERR_UNSUPPORTED
+
+
+# --------------------------------------------------------------------- append
+def test_kv_append_bit_exact(cf):
+    eng = engine_for(cf, wl.LLAMA8B)
+    pages, Hkv, d, n = 40, 8, 128, 300
+    kp = torch.full((pages, Hkv, 16, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vp = kp.clone()
+    slots = torch.as_tensor(np.random.default_rng(0).permutation(pages * 16)[:n].astype(np.int32), device="cuda")
+    k, v = randn_bf16((n, Hkv, d), 10), randn_bf16((n, Hkv, d), 11)
+    before_k = kp.view(torch.int16).cpu().numpy().copy()
+    eng.cf_kv_append(k, v, slots, cf.pool_of(kp, vp))
+    torch.cuda.synchronize()
+    # oracle scatter on the raw bit patterns
+    ref_k = before_k.copy()
+    ref_v = before_k.copy()
+    oracle.kv_append(ref_k, ref_v, k.view(torch.int16).cpu().numpy(), v.view(torch.int16).cpu().numpy(),
+                     slots.cpu().numpy(), 16)
+    assert np.array_equal(kp.view(torch.int16).cpu().numpy(), ref_k)
+    assert np.array_equal(vp.view(torch.int16).cpu().numpy(), ref_v)
+
+
+def test_kv_append_flags_bad_slot(cf):
+    eng = engine_for(cf, wl.TINY)
+    kp = torch.zeros((4, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    vp = kp.clone()
+    slots = torch.tensor([3, 4 * 16 + 5], dtype=torch.int32, device="cuda")
+    k, v = randn_bf16((2, 2, 64), 1), randn_bf16((2, 2, 64), 2)
+    eng.cf_kv_append(k, v, slots, cf.pool_of(kp, vp))
+    st, msg = eng.cf_get_error()
+    assert st == cf.CF_ERR_DEVICE and "page" in msg
+    assert torch.equal(kp[0, :, 3], k[0])          # the valid row still landed
+    assert eng.cf_get_error()[0] == 0              # the word was cleared
+
+
+# --------------------------------------------------------------------- decode
+DECODE_CASES = [
+    ("tiny", wl.TINY, (17, 64, 100, 255, 1, 16)),
+    ("l8b", wl.LLAMA8B, (5, 16, 17, 700, 1, 2049)),
+    ("q14b", wl.QWEN14B, (33, 1000, 15)),
+    ("q32b", wl.QWEN32B, (3000, 31, 64)),
+    ("g16", wl.LayerShape(2048, 32, 2, 64, 512, 1e4, 1e-5, False), (90, 1, 300)),
+]
+
+
+@pytest.mark.parametrize("name,shape,ctx", DECODE_CASES, ids=[c[0] for c in DECODE_CASES])
+@pytest.mark.parametrize("num_sms", [0, 3])
+def test_decode_attention_matches_oracle(cf, name, shape, ctx, num_sms):
+    w = wl.Workload(name, shape, len(ctx), ctx, 0, 0)
+    b = wl.make_batch(w, 1)
+    kp, vp = wl.make_pools(w, b, 1, "cuda")
+    n, Hq, d = len(ctx), shape.n_q_heads, shape.head_dim
+    q = randn_bf16((n, Hq, d), 12)
+    out = torch.zeros((n, Hq, d), dtype=torch.bfloat16, device="cuda")
+    eng = engine_for(cf, shape)
+    keys = torch.as_tensor(b.dec_ctx, device="cuda")        # positions 0..c_j-1 are cached
+    pages = torch.as_tensor(b.dec_pages, device="cuda")
+    ref = oracle.decode_attention(f64(q), kp, vp, b.dec_ctx, b.dec_pages, 16)
+    eng.cf_decode_attn(q, Hq * d, cf.pool_of(kp, vp), n, keys, pages, b.dec_stride, out, Hq * d, num_sms)
+    torch.cuda.synchronize()
+    assert eng.cf_get_error()[0] == 0
+    assert_close(out, ref, f"decode {name}")
+
+
+def test_decode_split_count_and_page_order_invariance(cf):
+    """Layout changes must not change results: a shuffled page table gives
+    bit-identical outputs; any split count agrees within fp32 rounding."""
+    shape = wl.LLAMA8B
+    ctx = (4000, 2500, 77)
+    w = wl.Workload("inv", shape, len(ctx), ctx, 0, 0)
+    b = wl.make_batch(w, 2)
+    kp, vp = wl.make_pools(w, b, 2, "cuda")
+    n, Hq, d = len(ctx), shape.n_q_heads, shape.head_dim
+    q = randn_bf16((n, Hq, d), 13)
+    eng = engine_for(cf, shape)
+    keys = torch.as_tensor(b.dec_ctx, device="cuda")
+    outs = {}
+    # identity layout: the same KV placed on pages in order
+    perm = np.argsort(np.random.default_rng(3).permutation(b.num_pages))
+    kp2 = torch.empty_like(kp); vp2 = torch.empty_like(vp)
+    ptab = b.dec_pages.copy()
+    valid = ptab >= 0
+    ptab[valid] = perm[ptab[valid]]
+    kp2[torch.as_tensor(perm, device="cuda")] = kp
+    vp2[torch.as_tensor(perm, device="cuda")] = vp
+    for tag, (K, V, tab) in {"a": (kp, vp, b.dec_pages), "b": (kp2, vp2, ptab)}.items():
+        for sms in (0, 7):
+            out = torch.zeros((n, Hq, d), dtype=torch.bfloat16, device="cuda")
+            eng.cf_decode_attn(q, Hq * d, cf.pool_of(K, V), n, keys, torch.as_tensor(tab, device="cuda"),
+                               b.dec_stride, out, Hq * d, sms)
+            outs[(tag, sms)] = out
+    torch.cuda.synchronize()
+    assert torch.equal(outs[("a", 0)], outs[("b", 0)])
+    assert torch.equal(outs[("a", 7)], outs[("b", 7)])
+    assert_close(outs[("a", 7)], f64(outs[("a", 0)]), "split count", 8e-3, 2e-4)
+
+
+# --------------------------------------------------------------------- prefill
+PREFILL_CASES = [
+    ("tiny", wl.TINY, 64, 128),
+    ("tiny-ragged", wl.TINY, 77, 5),
+    ("l8b", wl.LLAMA8B, 300, 0),
+    ("l8b-prefix", wl.LLAMA8B, 130, 333),
+    ("q14b", wl.QWEN14B, 1, 255),
+    ("q32b", wl.QWEN32B, 256, 1000),
+]
+
+
+@pytest.mark.parametrize("name,shape,l,cp", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_prefill_attention_matches_oracle(cf, name, shape, l, cp):
+    w = wl.Workload(name, shape, 0, (), l, cp)
+    b = wl.make_batch(w, 4)
+    kp, vp = wl.make_pools(w, b, 4, "cuda")
+    fill_positions(kp, vp, b.pre_pages, cp, l, 40)   # the chunk's own K/V (appended before attention)
+    Hq, d = shape.n_q_heads, shape.head_dim
+    q = randn_bf16((l, Hq, d), 14)
+    out = torch.zeros((l, Hq, d), dtype=torch.bfloat16, device="cuda")
+    eng = engine_for(cf, shape)
+    ref = oracle.prefill_attention(f64(q), kp, vp, cp, b.pre_pages, 16)
+    eng.cf_prefill_attn(q, cf.pool_of(kp, vp), l, cp, torch.as_tensor(b.pre_pages, device="cuda"), out)
+    torch.cuda.synchronize()
+    assert eng.cf_get_error()[0] == 0
+    assert_close(out, ref, f"prefill {name}")
+
+
+def test_prefill_equals_decode_for_last_row(cf):
+    """The last chunk row sees every key, exactly like a decode query."""
+    shape = wl.LLAMA8B
+    l, cp = 40, 1000
+    w = wl.Workload("pd", shape, 0, (), l, cp)
+    b = wl.make_batch(w, 5)
+    kp, vp = wl.make_pools(w, b, 5, "cuda")
+    fill_positions(kp, vp, b.pre_pages, cp, l, 50)
+    Hq, d = shape.n_q_heads, shape.head_dim
+    q = randn_bf16((l, Hq, d), 15)
+    eng = engine_for(cf, shape)
+    pages = torch.as_tensor(b.pre_pages, device="cuda")
+    out_p = torch.zeros((l, Hq, d), dtype=torch.bfloat16, device="cuda")
+    eng.cf_prefill_attn(q, cf.pool_of(kp, vp), l, cp, pages, out_p)
+    out_d = torch.zeros((1, Hq, d), dtype=torch.bfloat16, device="cuda")
+    keys = torch.tensor([cp + l], dtype=torch.int32, device="cuda")
+    eng.cf_decode_attn(q[l - 1:].contiguous(), Hq * d, cf.pool_of(kp, vp), 1, keys, pages[None].contiguous(),
+                       len(b.pre_pages), out_d, Hq * d)
+    torch.cuda.synchronize()
+    assert_close(out_p[l - 1:], f64(out_d), "prefill row vs decode", 1e-2, 1e-3)

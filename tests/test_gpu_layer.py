@@ -1,0 +1,335 @@
+"""GPU parity of the co-batched layer step against the fp64 oracle.
+
+Three kinds of checks:
+
+* stage-isolated parity (the gate): every stage of the layer runs through
+  the C ABI on the oracle's own bf16 inputs for that stage, and its output is
+  compared element by element with the oracle's output of the same stage, at
+  the layer tolerance (max e <= 2e-2, mean e <= 2e-3 with e = |gpu - ref| /
+  max(1, |ref|));
+* composition: cf_layer_step runs exactly those stage kernels — its
+  intermediate tensors equal the stage calls chained on the GPU bit for bit;
+* chained parity: cf_layer_step end to end against the oracle, with the
+  wider bound that the oracle's own sensitivity to last-bit differences
+  implies (each bf16 rounding between stages turns a last-bit difference
+  into an ulp flip that the random-weight FFN amplifies; see
+  tests/test_oracle.py::test_oracle_chain_sensitivity).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workload as wl
+from helpers import TOL_MAX, TOL_MEAN, LayerSetup, assert_close, errors, f64
+
+pytestmark = pytest.mark.gpu
+
+# chained bound: 5x the stage tolerance (the oracle itself moves `out` by up to
+# ~0.025 when one stage is perturbed by 2^-17 relative)
+CHAIN_MAX, CHAIN_MEAN = 0.1, 1e-2
+
+
+@pytest.fixture(scope="module")
+def cf():
+    import co_prefill_decode_gb300 as cf
+    cf.load_library()
+    return cf
+
+
+def bf16_dev(a):
+    return torch.as_tensor(np.ascontiguousarray(a), dtype=torch.float64).to(torch.bfloat16).cuda()
+
+
+def slots_of_rows(b, rows):
+    out = []
+    for r in rows:
+        if r < b.prefill_len:
+            out.append(int(oracle.slot_of(b.pre_pages, b.prefill_prefix + r, 16)))
+        else:
+            j = r - b.prefill_len
+            out.append(int(oracle.slot_of(b.dec_pages[j], int(b.dec_ctx[j]), 16)))
+    return np.asarray(out, np.int64)
+
+
+def read_slots(kp, vp, slots):
+    sl = torch.as_tensor(slots, device=kp.device)
+    return kp[sl // 16, :, sl % 16, :], vp[sl // 16, :, sl % 16, :]
+
+
+def stage_isolated(cf, S, rows=None):
+    """Runs each layer stage through the C ABI on the oracle's inputs."""
+    b, s, eng, W = S.b, S.s, S.eng, S.W
+    T, l = S.T, b.prefill_len
+    Hq, d, H = s.n_q_heads, s.head_dim, s.hidden
+    W64 = S.oracle_weights()
+    x64 = f64(S.x)
+    k0, v0 = S.kp.clone(), S.vp.clone()          # the cache before the step
+    ref = oracle.layer_step(x64, W64, s, b, k0, v0, rows=rows)
+    rr = ref["rows"]
+    res = {}
+
+    # a1: RMSNorm of x (all rows)
+    xn = torch.empty_like(S.x)
+    eng.cf_rmsnorm(S.x, W["g_attn"], xn)
+    xn_ref = oracle.bf16_round(oracle.rmsnorm(x64, W64.g_attn, s.rms_eps))
+    res["xn"] = errors(xn, xn_ref)
+
+    # a2: fused QKV on the oracle's xn (all rows), appending into a copy of the cache
+    kq, vq = k0.clone(), v0.clone()
+    q = torch.empty((T, Hq, d), dtype=torch.bfloat16, device="cuda")
+    eng.cf_qkv(S.batch, bf16_dev(xn_ref), cf.pool_of(kq, vq), q)
+    need = ref["need_rows"]
+    res["q"] = errors(q[need], ref["q_need"])
+    kn, vn = read_slots(kq, vq, slots_of_rows(b, need))
+    res["k"] = errors(kn, ref["k_need"])
+    res["v"] = errors(vn, ref["v_need"])
+
+    # a3 || a4: attention on the oracle's q, over a cache holding the oracle's k, v
+    ka, va = k0.clone(), v0.clone()
+    sl = torch.as_tensor(slots_of_rows(b, need), device="cuda")
+    ka[sl // 16, :, sl % 16, :] = bf16_dev(ref["k_need"])
+    va[sl // 16, :, sl % 16, :] = bf16_dev(ref["v_need"])
+    pool_a = cf.pool_of(ka, va)
+    q_need = bf16_dev(ref["q_need"])
+    attn_rows = []
+    npre = int(np.sum(need < l))
+    if npre:
+        qp = torch.zeros((l, Hq, d), dtype=torch.bfloat16, device="cuda")
+        qp[:npre] = q_need[:npre]
+        op = torch.zeros_like(qp)
+        eng.cf_prefill_attn(qp, pool_a, l, b.prefill_prefix, S.pre_pages, op)
+        attn_rows.append(op[:npre])
+    dec_sel = need[need >= l] - l
+    if len(dec_sel):
+        ds = torch.as_tensor(dec_sel, device="cuda")
+        keys = (S.dec_ctx[ds] + 1).contiguous()
+        od = torch.zeros((len(dec_sel), Hq, d), dtype=torch.bfloat16, device="cuda")
+        eng.cf_decode_attn(q_need[npre:].contiguous(), Hq * d, pool_a, len(dec_sel), keys,
+                           S.dec_pages[ds].contiguous(), b.dec_stride, od, Hq * d)
+        attn_rows.append(od)
+    attn_need = torch.cat(attn_rows)
+    where = np.searchsorted(need, rr)
+    res["attn"] = errors(attn_need[torch.as_tensor(where, device="cuda")], ref["attn"])
+
+    # a6: O-proj + residual on the oracle's attention output (selected rows)
+    a_o = bf16_dev(ref["attn"].reshape(len(rr), Hq * d))
+    h = torch.empty((len(rr), H), dtype=torch.float32, device="cuda")
+    eng.cf_gemm(a_o, W["w_o"], h, cf.CF_EPI_RESID_F32, aux=S.x[torch.as_tensor(rr, device="cuda")].contiguous())
+    res["h"] = errors(h, ref["h"])
+    # a7: RMSNorm of the oracle's h
+    h_o = torch.as_tensor(ref["h"], dtype=torch.float32).cuda()
+    hn = torch.empty((len(rr), H), dtype=torch.bfloat16, device="cuda")
+    eng.cf_rmsnorm(h_o, W["g_ffn"], hn)
+    res["hn"] = errors(hn, ref["hn"])
+    # a8: gate/up + SwiGLU on the oracle's hn
+    act = torch.empty((len(rr), s.ffn_dim), dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(bf16_dev(ref["hn"]), W["w_gate"], act, cf.CF_EPI_SWIGLU, aux=W["w_up"])
+    res["act"] = errors(act, ref["act"])
+    # a9: down + residual on the oracle's act and h
+    out = torch.empty((len(rr), H), dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(bf16_dev(ref["act"]), W["w_down"], out, cf.CF_EPI_RESID_BF16, aux=h_o)
+    res["out"] = errors(out, ref["out"])
+    torch.cuda.synchronize()
+    assert eng.cf_get_error()[0] == 0
+    report = "; ".join(f"{k}: max {m:.3g} mean {a:.3g}" for k, (m, a, _) in res.items())
+    bad = [k for k, (m, a, _) in res.items() if m > TOL_MAX or a > TOL_MEAN]
+    assert not bad, f"{bad} out of tolerance -- {report}"
+    return res
+
+
+def chained(S, rows=None):
+    """cf_layer_step end to end against the oracle chain."""
+    W64 = S.oracle_weights()
+    ref = oracle.layer_step(f64(S.x), W64, S.s, S.b, S.kp.cpu(), S.vp.cpu(), rows=rows)
+    out = S.step()
+    rr = ref["rows"]
+    T, Hq, d = S.T, S.s.n_q_heads, S.s.head_dim
+    kn, vn = read_slots(S.kp, S.vp, slots_of_rows(S.b, rr))
+    got = {
+        "q": (S.eng.buffer("q", T).view(T, Hq, d)[rr], ref["q"], TOL_MAX, TOL_MEAN),
+        "k": (kn, ref["k"], TOL_MAX, TOL_MEAN),
+        "v": (vn, ref["v"], TOL_MAX, TOL_MEAN),
+        "attn": (S.eng.buffer("attn", T)[rr], ref["attn"].reshape(len(rr), -1), TOL_MAX, TOL_MEAN),
+        "h": (S.eng.buffer("h", T)[rr], ref["h"], TOL_MAX, TOL_MEAN),
+        "out": (out[rr], ref["out"], CHAIN_MAX, CHAIN_MEAN),
+    }
+    res = {k: errors(g, r) for k, (g, r, _, _) in got.items()}
+    report = "; ".join(f"{k}: max {m:.3g} mean {a:.3g}" for k, (m, a, _) in res.items())
+    bad = [k for k, (g, r, tm, ta) in got.items() if res[k][0] > tm or res[k][1] > ta]
+    assert not bad, f"{bad} out of bound -- {report}"
+    return res
+
+
+SLICES = [
+    ("tiny", wl.WORKLOADS["tiny"]),
+    ("l8b", wl.reduced(wl.WORKLOADS["l8b"], (5, 300, 17, 1), 130, 0)),
+    ("q14b", wl.reduced(wl.WORKLOADS["q14b"], (40, 600), 200, 77)),
+    ("q32b", wl.reduced(wl.WORKLOADS["q32b"], (1000,), 64, 500)),
+    ("mix-decode-only", wl.reduced(wl.WORKLOADS["mix"], (700, 20, 3333), 0, 0)),
+    ("l8b-prefill-only", wl.reduced(wl.WORKLOADS["l8b"], (), 257, 31)),
+]
+
+
+@pytest.mark.parametrize("name,w", SLICES, ids=[s[0] for s in SLICES])
+def test_layer_stages_full_parity(cf, name, w):
+    """Every stage, every row and element, at sizes the oracle finishes in seconds."""
+    stage_isolated(cf, LayerSetup(w))
+
+
+@pytest.mark.parametrize("name,w", SLICES, ids=[s[0] for s in SLICES])
+def test_layer_chained_parity(cf, name, w):
+    chained(LayerSetup(w))
+
+
+FULL = ["l8b", "q14b", "mix", "q32b"]
+
+
+def sample_rows(b):
+    l, nd = b.prefill_len, b.n_decode
+    rng = np.random.default_rng(0)
+    return sorted(set([0, 1, min(127, l - 1), min(128, l - 1), l - 1] + list(rng.integers(0, l, 3)) +
+                      [l, l + nd - 1] + list(l + rng.integers(0, nd, 3))))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_layer_full_size_stages_sampled(cf, name):
+    """The measured workloads at full size; the oracle computes a sample of rows."""
+    S = LayerSetup(wl.WORKLOADS[name], gen_device="cuda")
+    stage_isolated(cf, S, rows=sample_rows(S.b))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_layer_full_size_chained_sampled(cf, name):
+    S = LayerSetup(wl.WORKLOADS[name], gen_device="cuda")
+    chained(S, rows=sample_rows(S.b))
+
+
+def test_layer_step_composes_the_stage_kernels(cf):
+    """cf_layer_step's intermediates equal the stage calls chained on the GPU."""
+    w = wl.reduced(wl.WORKLOADS["q14b"], (300, 45, 2000), 150, 60)
+    S = LayerSetup(w)
+    k0, v0 = S.kp.clone(), S.vp.clone()
+    out = S.step()
+    eng, W, T, s = S.eng, S.W, S.T, S.s
+    xn = torch.empty_like(S.x)
+    eng.cf_rmsnorm(S.x, W["g_attn"], xn)
+    assert torch.equal(xn, eng.buffer("xn", T))
+    q = torch.empty((T, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    eng.cf_qkv(S.batch, xn, cf.pool_of(k0, v0), q)
+    torch.cuda.synchronize()
+    assert torch.equal(q.view(T, -1), eng.buffer("q", T))
+    # same bits in every slot (the pools hold NaN sentinels, so compare the bit patterns)
+    assert torch.equal(k0.view(torch.int16), S.kp.view(torch.int16))
+    assert torch.equal(v0.view(torch.int16), S.vp.view(torch.int16))
+    l, nd = S.b.prefill_len, S.b.n_decode
+    attn = torch.empty((T, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    att_p = torch.empty((l, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    eng.cf_prefill_attn(q[:l].contiguous(), S.pool, l, S.b.prefill_prefix, S.pre_pages, att_p)
+    keys = (S.dec_ctx + 1).contiguous()
+    od = torch.empty((nd, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    eng.cf_decode_attn(q[l:].contiguous(), s.n_q_heads * s.head_dim, S.pool, nd, keys, S.dec_pages,
+                       S.b.dec_stride, od, s.n_q_heads * s.head_dim, eng.cf_engine_decode_sms())
+    attn[:l] = att_p
+    attn[l:] = od
+    assert torch.equal(attn.view(T, -1), eng.buffer("attn", T))
+    h = torch.empty((T, s.hidden), dtype=torch.float32, device="cuda")
+    eng.cf_gemm(attn.view(T, -1), W["w_o"], h, cf.CF_EPI_RESID_F32, aux=S.x)
+    assert torch.equal(h, eng.buffer("h", T))
+    hn = torch.empty_like(S.x)
+    eng.cf_rmsnorm(h, W["g_ffn"], hn)
+    assert torch.equal(hn, eng.buffer("hn", T))
+    act = torch.empty((T, s.ffn_dim), dtype=torch.bfloat16, device="cuda")
+    eng.cf_gemm(hn, W["w_gate"], act, cf.CF_EPI_SWIGLU, aux=W["w_up"])
+    assert torch.equal(act, eng.buffer("act", T))
+    o2 = torch.empty_like(S.x)
+    eng.cf_gemm(act, W["w_down"], o2, cf.CF_EPI_RESID_BF16, aux=h)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, out)
+
+
+def test_layer_tiny_untouched_slots(cf):
+    """The step writes exactly the T appended slots of the pool."""
+    S = LayerSetup(wl.WORKLOADS["tiny"])
+    before = S.kp.view(torch.int16).clone()
+    S.step()
+    changed = (S.kp.view(torch.int16) != before).any(dim=-1)
+    expect = np.zeros(changed.shape, bool)
+    for sl in slots_of_rows(S.b, range(S.T)):
+        expect[sl // 16, :, sl % 16] = True
+    assert np.array_equal(changed.cpu().numpy(), expect)
+
+
+def test_layer_page_permutation_invariance(cf):
+    """Moving the same KV to other pages (and the tables with it) gives
+    bit-identical outputs."""
+    w = wl.reduced(wl.WORKLOADS["l8b"], (200, 1000, 33), 100, 50)
+    S1 = LayerSetup(w)
+    out1 = S1.step().clone()
+    S2 = LayerSetup(w)
+    perm = np.random.default_rng(9).permutation(S2.b.num_pages)
+    pt = torch.as_tensor(perm, device="cuda")
+    kp2 = torch.empty_like(S2.kp)
+    vp2 = torch.empty_like(S2.vp)
+    kp2[pt] = S2.kp
+    vp2[pt] = S2.vp
+    S2.kp.copy_(kp2)
+    S2.vp.copy_(vp2)
+    dp = S2.b.dec_pages.copy()
+    dp[dp >= 0] = perm[dp[dp >= 0]]
+    S2.dec_pages.copy_(torch.as_tensor(dp, device="cuda"))
+    S2.pre_pages.copy_(torch.as_tensor(perm[S2.b.pre_pages], device="cuda"))
+    out2 = S2.step()
+    assert torch.equal(out1, out2)
+
+
+def test_layer_cobatched_rows_match_separate_batches(cf):
+    """ConfluxServe §4: rows of the co-batched step equal the same rows run
+    as a prefill-only and a decode-only step over the same cache.  Prefill
+    rows are bit-identical (GEMM rows are independent, attention items do not
+    depend on the grid); decode rows may split the keys differently, so they
+    agree within fp32 rounding."""
+    base = wl.WORKLOADS["l8b"]
+    dec, l, cp = (300, 64), 96, 40
+    S = LayerSetup(wl.reduced(base, dec, l, cp))
+    out = S.step().clone()
+    xp, xd = S.x[:l].contiguous(), S.x[l:].contiguous()
+    op, od = torch.empty_like(xp), torch.empty_like(xd)
+    S.eng.cf_layer_step(cf.batch_of(0, None, None, l, cp, S.pre_pages), xp, op, S.pool)
+    S.eng.cf_layer_step(cf.batch_of(len(dec), S.dec_ctx, S.dec_pages, 0, 0, S.pre_pages), xd, od, S.pool)
+    torch.cuda.synchronize()
+    assert S.eng.cf_get_error()[0] == 0
+    assert torch.equal(op, out[:l])
+    assert_close(od, f64(out[l:]), "decode rows", 1e-2, 1e-3)
+
+
+def test_layer_flags_bad_page_id(cf):
+    w = wl.reduced(wl.WORKLOADS["tiny"], (17, 40), 16, 0)
+    S = LayerSetup(w)
+    S.dec_pages[1, 0] = S.b.num_pages + 5        # outside the pool
+    S.eng.cf_layer_step(S.batch, S.x, S.out, S.pool)
+    st, msg = S.eng.cf_get_error()
+    assert st == cf.CF_ERR_DEVICE and "page" in msg
+    # the engine stays usable
+    S.dec_pages[1, 0] = int(S.b.dec_pages[1, 0])
+    S.step()
+
+
+def test_layer_rejects_bad_arguments(cf):
+    w = wl.reduced(wl.WORKLOADS["tiny"], (17,), 8, 0)
+    S = LayerSetup(w)
+    big = cf.batch_of(1, S.dec_ctx, S.dec_pages, S.cfg.max_tokens + 1, 0, S.pre_pages)
+    with pytest.raises(cf.CfError) as e:
+        S.eng.cf_layer_step(big, S.x, S.out, S.pool)
+    assert e.value.status == cf.CF_ERR_INVALID_ARG
+    with pytest.raises(cf.CfError):
+        S.eng.cf_layer_step(S.batch, S.x, S.x, S.pool)      # in place is not allowed
+
+
+def test_layer_step_is_deterministic_and_launch_count(cf):
+    S = LayerSetup(wl.reduced(wl.WORKLOADS["q14b"], (100, 9), 50, 10))
+    n0 = S.eng.cf_launch_count()
+    a = S.step().clone()
+    assert S.eng.cf_launch_count() - n0 == 9
+    b = S.step()
+    assert torch.equal(a, b)

@@ -356,3 +356,32 @@ def test_qk_norm_is_per_head_over_head_dim():
     for t in (r["q"][0], r["k"][0]):
         rms = np.sqrt((t * t).mean(-1))
         assert np.allclose(rms, 1.0, atol=4e-3)
+
+
+def test_oracle_chain_sensitivity(monkeypatch):
+    """How far two correct bf16-boundary implementations of the layer can drift
+    apart when compared end to end: perturbing only the attention output by a
+    relative 2^-17 (far below one bf16 ulp) moves the final output by up to
+    ~1e-2 of max(1, |ref|), because each later bf16 rounding turns the
+    difference into ulp flips that the FFN amplifies.  This is why the GPU
+    layer is gated stage by stage and the chained comparison gets a wider
+    bound (tests/test_gpu_layer.py)."""
+    from oracle import layer as L
+    w = wl.reduced(wl.WORKLOADS["l8b"], (5, 300, 17, 1), 130, 0)
+    b = wl.make_batch(w)
+    x = oracle.to_f64(wl.make_x(w, b))
+    W = oracle.LayerWeights64.from_torch(wl.make_weights(w))
+    kp, vp = wl.make_pools(w, b)
+    kp, vp = oracle.to_f64(kp), oracle.to_f64(vp)
+    ref = L.layer_step(x, W, w.shape, b, kp, vp)
+    orig = L.attention
+    rng = np.random.default_rng(0)
+
+    def perturbed(*a, **k):
+        o = orig(*a, **k)
+        return o * (1.0 + rng.uniform(-1, 1, o.shape) * 2.0 ** -17)
+
+    monkeypatch.setattr(L, "attention", perturbed)
+    got = L.layer_step(x, W, w.shape, b, kp, vp)
+    e = np.abs(got["out"] - ref["out"]) / np.maximum(1.0, np.abs(ref["out"]))
+    assert 2e-3 < e.max() < 0.1 and e.mean() < 1e-2
