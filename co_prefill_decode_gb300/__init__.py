@@ -27,7 +27,7 @@ EXPORTS = (
     "cf_device_sm_count", "cf_create", "cf_destroy", "cf_layer_step", "cf_decode_attn",
     "cf_prefill_attn", "cf_gemm", "cf_kv_append", "cf_get_error", "cf_engine_buffer",
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
-    "cf_launch_count", "cf_rmsnorm", "cf_qkv",
+    "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc",
 )
 
 
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_get_phase_times": (I, [P, ctypes.POINTER(F), I, ctypes.POINTER(I)]),
         "cf_launch_count": (L, [P]),
         "cf_rmsnorm": (I, [P, P, I, P, P, I, P]),
+        "cf_decode_attn_noalloc": (I, [I, I, I, I, P, L, ctypes.POINTER(cf_kv_pool), I, P, P, I, P, L, I, P]),
         "cf_qkv": (I, [P, ctypes.POINTER(cf_batch), P, ctypes.POINTER(cf_kv_pool), P, P]),
     }
     for name, (res, args) in sig.items():
@@ -243,6 +244,19 @@ class _DeviceArray:
     def __init__(self, ptr: int, shape, typestr: str):
         self.__cuda_array_interface__ = {"data": (int(ptr), False), "shape": tuple(shape),
                                          "typestr": typestr, "version": 3, "strides": None}
+
+
+def cf_decode_attn_noalloc(n_q_heads: int, n_kv_heads: int, head_dim: int, page_size: int, q,
+                           q_row_stride: int, pool: cf_kv_pool, n: int, n_keys, pages, page_stride: int, out,
+                           out_row_stride: int, num_sms: int = 0, stream=None):
+    """Decode attention with no engine and no allocation (scratch lives in a
+    fixed array inside the library); see include/cf.h."""
+    lib = load_library()
+    st = lib.cf_decode_attn_noalloc(n_q_heads, n_kv_heads, head_dim, page_size, _ptr(q), q_row_stride,
+                                    ctypes.byref(pool), n, _ptr(n_keys), _ptr(pages), page_stride, _ptr(out),
+                                    out_row_stride, num_sms, _stream(stream))
+    if st != CF_OK:
+        raise CfError(st, "cf_decode_attn_noalloc")
 
 
 def pool_of(k_pool: torch.Tensor, v_pool: torch.Tensor) -> cf_kv_pool:

@@ -198,6 +198,32 @@ cf_status cf_gemm(cf_engine* e, const void* A, int lda, const void* B, int ldb,
                   void* C, int ldc, int M, int N, int K, int epilogue,
                   const void* aux, void* stream);
 
+/* Decode attention that allocates nothing.  The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * a serving runtime whose own pool already holds all free device memory, a
+ * plugin inside a framework whose allocator owns the device, or a loop that
+ * must never pay for cudaMalloc's device-wide synchronisation -- and so can
+ * create no engine.  It computes exactly what cf_decode_attn computes (same
+ * kernel, same arguments, shape passed explicitly) but keeps its split-K
+ * scratch in a 16 MiB array compiled into the library, which every GPU that
+ * loads the library holds until the process exits.
+ * - The first call on each device looks up that array's device address
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ * - Batches whose scratch would exceed 16 MiB are rejected with
+ *   CF_ERR_INVALID_ARG (the need grows with n * Hkv and with the number of
+ *   CTAs; a smaller num_sms lowers it).
+ * - All calls share the one array, which keeps the last call's contents
+ *   (nothing in it has to start at zero): calls that may overlap on the GPU,
+ *   e.g. on two streams, race and must be serialised by the caller.
+ * - Device-side problems (a page id outside the pool) are skipped as in
+ *   cf_decode_attn but are not reported, since there is no engine error word.
+ * It calls no cudaMalloc, cudaFree or allocating library routine. */
+cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                                 const void* q, long long q_row_stride, const cf_kv_pool* pool, int n,
+                                 const int* n_keys, const int* pages, int page_stride, void* out,
+                                 long long out_row_stride, int num_sms, void* stream);
+
 /* Paged KV append (ConfluxServe §4, Fig. 8: each request extends its own KV
  * cache with its new tokens).  k, v: bf16 [n][Hkv][d]; slots: device int32
  * [n] = page * page_size + offset.  Row r is copied bit for bit to
