@@ -223,6 +223,15 @@ def run_cf(args, rank, world, local, pg):
     st, msg = eng.cf_get_error()
     if st != 0:
         raise RuntimeError(msg)
+    calib = None
+    if args.decode_sms == 0 and b.n_decode > 0 and b.prefill_len > 0:
+        # ConfluxServe §6.1: decode gets the fewest SMs that keep 90% of its solo bandwidth
+        chosen = eng.cf_calibrate_decode_sms(batch, pool, 0.9)
+        calib = {"rule": "min SMs reaching 90% of standalone decode bandwidth", "chosen": chosen,
+                 "points": [{"sms": n, "ms": round(t, 4)} for n, t in eng.cf_calibration_points()]}
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -319,6 +328,7 @@ def run_cf(args, rank, world, local, pg):
         "gemm_tflops": gemm_tflops,
         "fork_vs_serial": per["fork"] / max(1e-9, per["decode"] + per["prefill"]),
         "kernels": kern,
+        "decode_sms_calibration": calib,
         "roofline": roofline,
         "e2e": {"value": tok_total / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -359,6 +369,63 @@ def sweep_decode_sms(eng, step, args, cf):
     return res
 
 
+# ------------------------------------------------------------------ single launches for ncu
+def run_kernel_case(args):
+    """One small launch of one kernel (plus a warm-up launch), for profilers.
+
+    decode : decode attention, Qwen3-32B shape, 8 requests x 8192 cached keys
+             (268 MB of KV, larger than L2)
+    prefill: prefill attention, Qwen3-32B shape, 512-token chunk on 4096 cached
+    gemm   : gate/up GEMM + SwiGLU epilogue of the Llama-3.1-8B layer, T = 1040
+    """
+    import numpy as np
+    import torch
+
+    import co_prefill_decode_gb300 as cf
+    import workload as wl
+    which = args.kernel
+    s = wl.LLAMA8B if which == "gemm" else wl.QWEN32B
+    if which == "decode":
+        w = wl.Workload("k", s, 8, (8192,) * 8, 0, 0)
+    elif which == "prefill":
+        w = wl.Workload("k", s, 0, (), 512, 4096)
+    else:
+        w = wl.Workload("k", s, 0, (), 1040, 0)
+    b = wl.make_batch(w, args.seed)
+    kp, vp = wl.make_pools(w, b, args.seed, "cuda")
+    W = wl.make_weights(wl.Workload("k", s, 1, (1,), 0, 0), args.seed, "cuda", unit_gains=True)
+    eng = cf.Engine(cf.make_config(s, 2048, 64), W)
+    pool = cf.pool_of(kp, vp)
+    Hq, d = s.n_q_heads, s.head_dim
+    g = torch.Generator(device="cuda").manual_seed(args.seed)
+    if which == "prefill":
+        l, cp = b.prefill_len, b.prefill_prefix
+        pos = np.arange(cp, cp + l)
+        pg = torch.as_tensor(b.pre_pages[pos // 16].astype(np.int64), device="cuda")
+        off = torch.as_tensor(pos % 16, device="cuda")
+        kp[pg, :, off, :] = torch.randn(l, s.n_kv_heads, d, device="cuda", generator=g).bfloat16()
+        vp[pg, :, off, :] = torch.randn(l, s.n_kv_heads, d, device="cuda", generator=g).bfloat16()
+    for _ in range(2):
+        if which == "decode":
+            q = torch.randn(b.n_decode, Hq, d, device="cuda", generator=g).bfloat16()
+            o = torch.empty_like(q)
+            eng.cf_decode_attn(q, Hq * d, pool, b.n_decode, torch.as_tensor(b.dec_ctx, device="cuda"),
+                               torch.as_tensor(b.dec_pages, device="cuda"), b.dec_stride, o, Hq * d)
+        elif which == "prefill":
+            q = torch.randn(b.prefill_len, Hq, d, device="cuda", generator=g).bfloat16()
+            o = torch.empty_like(q)
+            eng.cf_prefill_attn(q, pool, b.prefill_len, b.prefill_prefix, torch.as_tensor(b.pre_pages, device="cuda"), o)
+        else:
+            A = torch.randn(1040, s.hidden, device="cuda", generator=g).bfloat16()
+            C = torch.empty(1040, s.ffn_dim, device="cuda").bfloat16()
+            eng.cf_gemm(A, W["w_gate"], C, cf.CF_EPI_SWIGLU, aux=W["w_up"])
+    torch.cuda.synchronize()
+    st, msg = eng.cf_get_error()
+    if st != 0:
+        raise RuntimeError(msg)
+    return {"kernel_case": which, "ok": True}
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
     import workload as wl
@@ -396,9 +463,14 @@ def main(argv=None):
     ap.add_argument("--decode-sms", type=int, default=0)
     ap.add_argument("--sweep-decode-sms", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["decode", "prefill", "gemm"], default=None,
+                    help="run one small launch of one kernel (for ncu) instead of the benchmark")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.kernel:
+        print(json.dumps(run_kernel_case(args)))
+        return
     rank, world, local, pg = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, rank, world)

@@ -27,7 +27,8 @@ EXPORTS = (
     "cf_device_sm_count", "cf_create", "cf_destroy", "cf_layer_step", "cf_decode_attn",
     "cf_prefill_attn", "cf_gemm", "cf_kv_append", "cf_get_error", "cf_engine_buffer",
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
-    "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc",
+    "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
+    "cf_calibration_points",
 )
 
 
@@ -88,6 +89,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_get_phase_times": (I, [P, ctypes.POINTER(F), I, ctypes.POINTER(I)]),
         "cf_launch_count": (L, [P]),
         "cf_rmsnorm": (I, [P, P, I, P, P, I, P]),
+        "cf_calibrate_decode_sms": (I, [P, ctypes.POINTER(cf_batch), ctypes.POINTER(cf_kv_pool), F, P,
+                                        ctypes.POINTER(I)]),
+        "cf_calibration_points": (I, [P, ctypes.POINTER(I), ctypes.POINTER(F), I]),
         "cf_decode_attn_noalloc": (I, [I, I, I, I, P, L, ctypes.POINTER(cf_kv_pool), I, P, P, I, P, L, I, P]),
         "cf_qkv": (I, [P, ctypes.POINTER(cf_batch), P, ctypes.POINTER(cf_kv_pool), P, P]),
     }
@@ -197,6 +201,19 @@ class Engine:
     def cf_qkv(self, batch: cf_batch, xn, pool: cf_kv_pool, q_out, stream=None):
         _check(self.lib, self.handle, self.lib.cf_qkv(self.handle, ctypes.byref(batch), _ptr(xn),
                                                       ctypes.byref(pool), _ptr(q_out), _stream(stream)))
+
+    def cf_calibrate_decode_sms(self, batch: cf_batch, pool: cf_kv_pool, frac: float = 0.9, stream=None) -> int:
+        out = ctypes.c_int()
+        _check(self.lib, self.handle, self.lib.cf_calibrate_decode_sms(
+            self.handle, ctypes.byref(batch), ctypes.byref(pool), frac, _stream(stream), ctypes.byref(out)))
+        return out.value
+
+    def cf_calibration_points(self):
+        n = self.lib.cf_calibration_points(self.handle, None, None, 0)
+        sms = (ctypes.c_int * max(n, 1))()
+        ms = (ctypes.c_float * max(n, 1))()
+        self.lib.cf_calibration_points(self.handle, sms, ms, n)
+        return [(sms[i], ms[i]) for i in range(n)]
 
     def cf_get_error(self):
         buf = ctypes.create_string_buffer(512)

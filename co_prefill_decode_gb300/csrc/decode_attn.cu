@@ -6,15 +6,19 @@
 // (request j, KV head h, chunk of pages); one warp serves all G query heads
 // of KV head h, so each 4 KB (page, head) tile is streamed once.
 //
-// Each lane loads 16-byte vectors straight from HBM into registers (the
-// next page's loads are issued before the current page is processed), and
-// the two small contractions per page, S = Q_g K^T (G x 16 keys) and
+// Loads: one lane of each warp issues TMA tensor copies of the page's K and
+// V tiles (16 rows x 64 columns per box, 128-byte swizzle) into a per-warp
+// ring of page slots, completed on one mbarrier per slot, so the bytes in
+// flight are bounded by shared memory rather than by the SM's outstanding
+// load slots.  Fragments are then read with ldmatrix (K) and ldmatrix.trans
+// (V), which the swizzle makes bank-conflict free.
+//
+// The two small contractions per page, S = Q_g K^T (G x 16 keys) and
 // O += P V (G x d), run on mma.sync m16n8k16 with the G query heads as the
-// M rows: G = 4..8 rows would need 2-8x more CUDA-core FMAs than the HBM
-// stream allows when decode owns only part of the SMs.  The register
-// layouts are chosen so that K feeds the B fragment directly (a fixed
-// permutation of d shared by Q and K leaves the dot products unchanged) and
-// V feeds it after one byte-permute, with no shared-memory staging.
+// M rows: with only part of the SMs, G = 4..8 rows of CUDA-core FMAs per
+// key would not keep up with the HBM stream.  For G <= 8 the otherwise
+// padded rows 8..15 of the P V product carry the low bf16 half of P
+// (P = hi + lo), so P V is accurate to ~2^-16 at no extra MMA cost.
 //
 // Partial results (unnormalised O, running max m in log2 units, sum l) of
 // the chunks of one (request, head) are merged with the log-sum-exp rule
@@ -28,8 +32,41 @@ namespace cf {
 namespace {
 
 constexpr int kThreads = kDecodeWarps * 32;
-constexpr int kDecodeSmem = 64 * 1024;   // also keeps decode CTAs off prefill SMs
-constexpr int kItemsPerWarp = 3;
+constexpr int kMaxDecodeReqs = 2048;                 // plan arrays in shared memory
+// plan arrays, padded so that the page ring after them starts 1 KB aligned
+// (the 128-byte swizzle repeats every 1024 bytes)
+constexpr int kPlanBytes = (((2 * kMaxDecodeReqs + 2) * 4 + 1023) / 1024) * 1024;
+constexpr int kRingBytes = 192 * 1024;               // per CTA, split over the warps
+constexpr int kBarBytes = 1024;                      // per-slot mbarriers
+// + 1 KB so the base can be aligned to 1 KB by hand; > half an SM, so a decode
+// CTA never shares an SM with a prefill CTA
+constexpr int kDecodeSmem = kPlanBytes + kRingBytes + kBarBytes + 1024;
+constexpr int kItemsPerWarp = 4;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: O is rescaled only when the max grows more
+
+template <int D>
+struct Ring {
+  static constexpr int HALF = 16 * 128;                // one 16 x 64 box (2 KB)
+  static constexpr int KV = HALF * (D / 64);           // K (or V) tile of one page
+  static constexpr int PAGE = 2 * KV;                  // 8 KB for d = 128
+  static constexpr int STAGES = kRingBytes / kDecodeWarps / PAGE;
+  static_assert(STAGES >= 2 && STAGES * kDecodeWarps * 8 <= kBarBytes, "ring shape");
+  static_assert(kPlanBytes % 1024 == 0 && PAGE % 1024 == 0, "swizzled boxes need 1 KB alignment");
+};
+
+// byte offset of 16-byte chunk c (of d) in row r of a swizzled K or V tile
+CF_DEV uint32_t swz(int r, int c) { return (c >> 3) * (16 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4); }
+
+CF_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+CF_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
 
 CF_DEV void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -38,76 +75,45 @@ CF_DEV void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-CF_DEV uint32_t word(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
-CF_DEV uint32_t pair_lo(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410); }
-CF_DEV uint32_t pair_hi(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
-
-template <int D>
-struct PageRegs {
-  uint4 k[2][D / 32];   // n-tile (8 keys), 16-byte chunk (4jj + t)
-  uint4 v[4][D / 64];   // keys 2t, 2t+1, 2t+8, 2t+9; d block 64*half + 8g
-  int valid;            // keys of this page that exist (0..16)
-};
-
-template <int D>
-CF_DEV void load_page(PageRegs<D>& r, const DecodeArgs& a, const int* table, int p, int keys, int h, int g, int t) {
-  const int pid = table[p];
-  int valid = keys - p * 16;
-  valid = valid > 16 ? 16 : valid;
-  if (pid < 0 || pid >= a.num_pages) {
-    if ((threadIdx.x & 31) == 0) set_error(a.err, CF_DEVERR_PAGE);
-    valid = 0;
-  }
-  r.valid = valid;
-  if (valid <= 0) {
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int jj = 0; jj < D / 32; ++jj) r.k[n][jj] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh) r.v[kk][hh] = make_uint4(0, 0, 0, 0);
-    return;
-  }
-  const size_t base = ((size_t)pid * a.Hkv + h) * 16 * D;
-  const __nv_bfloat16* kb = a.k_pool + base;
-  const __nv_bfloat16* vb = a.v_pool + base;
-#pragma unroll
-  for (int n = 0; n < 2; ++n)
-#pragma unroll
-    for (int jj = 0; jj < D / 32; ++jj) r.k[n][jj] = ldg_stream(kb + (n * 8 + g) * D + (4 * jj + t) * 8);
-  const int keys4[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-    for (int hh = 0; hh < D / 64; ++hh) r.v[kk][hh] = ldg_stream(vb + keys4[kk] * D + hh * 64 + 8 * g);
-}
 
 template <int D, bool G16>
 struct Acc {
-  float o[D / 8][2];      // row g: d = 64*(m/8) + 16t + (m%8) [+8]
+  float o[D / 8][2];      // row g: d = 8 m + 2 t, +1
   float o8[D / 8][2];     // row g + 8: heads 8..15 (G > 8) or the low part of P (G <= 8)
   float m0, l0, m1, l1;
 };
 
+// One page (16 keys) of one item: S = Q K^T, online softmax, O += P V.
+// kt, vt: shared-memory addresses of the page's K and V tiles.
 template <int D, bool G16>
-CF_DEV void process_page(Acc<D, G16>& A, PageRegs<D>& r, const uint32_t (*qa)[2], const uint32_t (*qb)[2],
-                         float scale_log2, int t) {
-  // ---- S = Q K^T for two n-tiles of 8 keys
+CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
+                         const uint32_t (*qb)[2], float scale_log2, int lane) {
+  const int t = lane & 3;
+  // ---- S = Q K^T: two n-tiles of 8 keys, two accumulator chains each
   float s[2][4];
+  {
+    float e0[2][4], e1[2][4];
 #pragma unroll
-  for (int n = 0; n < 2; ++n) {
-    s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
-    for (int st = 0; st < D / 16; ++st) {
-      const uint4& kv = r.k[n][st >> 1];
-      const uint32_t b0 = word(kv, (st & 1) * 2), b1 = word(kv, (st & 1) * 2 + 1);
-      mma16816(s[n], qa[st][0], G16 ? qb[st][0] : 0u, qa[st][1], G16 ? qb[st][1] : 0u, b0, b1);
-    }
+      for (int i = 0; i < 4; ++i) e0[n][i] = e1[n][i] = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < D / 32; ++sp)
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        uint32_t b[4];
+        ldsm_x4(kt + swz(8 * n + (lane & 7), 4 * sp + (lane >> 3)), b[0], b[1], b[2], b[3]);
+        mma16816(e0[n], qa[2 * sp][0], G16 ? qb[2 * sp][0] : 0u, qa[2 * sp][1], G16 ? qb[2 * sp][1] : 0u, b[0],
+                 b[1]);
+        mma16816(e1[n], qa[2 * sp + 1][0], G16 ? qb[2 * sp + 1][0] : 0u, qa[2 * sp + 1][1],
+                 G16 ? qb[2 * sp + 1][1] : 0u, b[2], b[3]);
+      }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[n][i] = e0[n][i] + e1[n][i];
   }
   // ---- mask, scale, online softmax (log2 domain)
-  const int valid = r.valid;
   float x[2][2], y[2][2];
 #pragma unroll
   for (int n = 0; n < 2; ++n)
@@ -120,9 +126,26 @@ CF_DEV void process_page(Acc<D, G16>& A, PageRegs<D>& r, const uint32_t (*qa)[2]
   float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-  const float mnew = fmaxf(A.m0, mx);
-  const float muse = mnew == -INFINITY ? 0.f : mnew;
-  const float alpha = fast_exp2(A.m0 - muse);
+  // lazy rescaling: keep the running max unless it grows by more than 2^8
+  // (P then stays below 256, exact enough in fp32 and in the bf16 hi/lo split)
+  const bool first = A.m0 == -INFINITY;
+  const bool grow = !first && mx > A.m0 + kRescaleThreshold;
+  if (first) A.m0 = mx;
+  if (__any_sync(0xffffffffu, grow)) {
+    const float alpha = grow ? fast_exp2(A.m0 - mx) : 1.0f;
+    if (grow) A.m0 = mx;
+    A.l0 *= alpha;
+#pragma unroll
+    for (int m = 0; m < D / 8; ++m) {
+      A.o[m][0] *= alpha;
+      A.o[m][1] *= alpha;
+      if constexpr (!G16) {
+        A.o8[m][0] *= alpha;
+        A.o8[m][1] *= alpha;
+      }
+    }
+  }
+  const float muse = A.m0 == -INFINITY ? 0.f : A.m0;
   float p[2][2];
   float ls = 0.f;
 #pragma unroll
@@ -132,27 +155,32 @@ CF_DEV void process_page(Acc<D, G16>& A, PageRegs<D>& r, const uint32_t (*qa)[2]
       p[n][e] = fast_exp2(x[n][e] - muse);
       ls += p[n][e];
     }
-  A.l0 = A.l0 * alpha + ls;
-  A.m0 = mnew;
-#pragma unroll
-  for (int m = 0; m < D / 8; ++m) {
-    A.o[m][0] *= alpha;
-    A.o[m][1] *= alpha;
-  }
-  // P is split into bf16 high and low parts so that P V is accurate to
-  // ~2^-16 relative: P ~= hi + lo, hi = bf16(P), lo = bf16(P - hi).
+  A.l0 += ls;
+  // P is split into bf16 high and low parts: P ~= hi + lo, hi = bf16(P),
+  // lo = bf16(P - hi).
   const uint32_t pa0 = pack_bf16(p[0][0], p[0][1]), pa2 = pack_bf16(p[1][0], p[1][1]);
   const uint32_t pl0 = pack_bf16(p[0][0] - bf16lo(pa0), p[0][1] - bf16hi(pa0));
   const uint32_t pl2 = pack_bf16(p[1][0] - bf16lo(pa2), p[1][1] - bf16hi(pa2));
   uint32_t pa1 = pl0, pa3 = pl2;     // G <= 8: rows g+8 of the MMA carry the low part
-  uint32_t qa1 = 0u, qa3 = 0u, ql1 = 0u, ql3 = 0u;
+  uint32_t ql1 = 0u, ql3 = 0u;
   if constexpr (G16) {
     float my = fmaxf(fmaxf(y[0][0], y[0][1]), fmaxf(y[1][0], y[1][1]));
     my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
     my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
-    const float m1n = fmaxf(A.m1, my);
-    const float m1u = m1n == -INFINITY ? 0.f : m1n;
-    const float a1 = fast_exp2(A.m1 - m1u);
+    const bool first1 = A.m1 == -INFINITY;
+    const bool grow1 = !first1 && my > A.m1 + kRescaleThreshold;
+    if (first1) A.m1 = my;
+    if (__any_sync(0xffffffffu, grow1)) {
+      const float a1 = grow1 ? fast_exp2(A.m1 - my) : 1.0f;
+      if (grow1) A.m1 = my;
+      A.l1 *= a1;
+#pragma unroll
+      for (int m = 0; m < D / 8; ++m) {
+        A.o8[m][0] *= a1;
+        A.o8[m][1] *= a1;
+      }
+    }
+    const float m1u = A.m1 == -INFINITY ? 0.f : A.m1;
     float q[2][2], lq = 0.f;
 #pragma unroll
     for (int n = 0; n < 2; ++n)
@@ -161,84 +189,52 @@ CF_DEV void process_page(Acc<D, G16>& A, PageRegs<D>& r, const uint32_t (*qa)[2]
         q[n][e] = fast_exp2(y[n][e] - m1u);
         lq += q[n][e];
       }
-    A.l1 = A.l1 * a1 + lq;
-    A.m1 = m1n;
-#pragma unroll
-    for (int m = 0; m < D / 8; ++m) {
-      A.o8[m][0] *= a1;
-      A.o8[m][1] *= a1;
-    }
-    qa1 = pack_bf16(q[0][0], q[0][1]);
-    qa3 = pack_bf16(q[1][0], q[1][1]);
-    ql1 = pack_bf16(q[0][0] - bf16lo(qa1), q[0][1] - bf16hi(qa1));
-    ql3 = pack_bf16(q[1][0] - bf16lo(qa3), q[1][1] - bf16hi(qa3));
-    pa1 = qa1;
-    pa3 = qa3;
-  } else {
-#pragma unroll
-    for (int m = 0; m < D / 8; ++m) {
-      A.o8[m][0] *= alpha;
-      A.o8[m][1] *= alpha;
-    }
+    A.l1 += lq;
+    pa1 = pack_bf16(q[0][0], q[0][1]);
+    pa3 = pack_bf16(q[1][0], q[1][1]);
+    ql1 = pack_bf16(q[0][0] - bf16lo(pa1), q[0][1] - bf16hi(pa1));
+    ql3 = pack_bf16(q[1][0] - bf16lo(pa3), q[1][1] - bf16hi(pa3));
   }
-  // ---- zero V of keys past the end (their slots may hold anything)
+  // keys past the end of the request: their V (any bits, even NaN) must not
+  // reach the product, so zero those halves of the B fragments
+  uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
   if (valid < 16) {
-    const int keys4[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      if (keys4[kk] >= valid)
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) r.v[kk][hh] = make_uint4(0, 0, 0, 0);
+    vm0 = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+    vm1 = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
   }
-  // ---- O += P V, n-tile m covers d = 64*(m/8) + 8*col + (m%8)
+  // ---- O += P V, two n-tiles (16 d) per ldmatrix.x4.trans
 #pragma unroll
-  for (int m = 0; m < D / 8; ++m) {
-    const int hh = m >> 3, e = m & 7;
-    const uint32_t w0 = word(r.v[0][hh], e >> 1), w1 = word(r.v[1][hh], e >> 1);
-    const uint32_t w2 = word(r.v[2][hh], e >> 1), w3 = word(r.v[3][hh], e >> 1);
-    const uint32_t b0 = (e & 1) ? pair_hi(w0, w1) : pair_lo(w0, w1);
-    const uint32_t b1 = (e & 1) ? pair_hi(w2, w3) : pair_lo(w2, w3);
-    float c[4] = {A.o[m][0], A.o[m][1], A.o8[m][0], A.o8[m][1]};
-    mma16816(c, pa0, pa1, pa2, pa3, b0, b1);
-    if constexpr (G16) mma16816(c, pl0, ql1, pl2, ql3, b0, b1);   // low parts of both row groups
-    A.o[m][0] = c[0];
-    A.o[m][1] = c[1];
-    A.o8[m][0] = c[2];
-    A.o8[m][1] = c[3];
+  for (int m = 0; m < D / 8; m += 2) {
+    uint32_t b[4];
+    ldsm_x4_t(vt + swz((lane & 7) + 8 * ((lane >> 3) & 1), m + (lane >> 4)), b[0], b[1], b[2], b[3]);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t b0 = b[2 * u] & vm0, b1 = b[2 * u + 1] & vm1;
+      float c[4] = {A.o[m + u][0], A.o[m + u][1], A.o8[m + u][0], A.o8[m + u][1]};
+      mma16816(c, pa0, pa1, pa2, pa3, b0, b1);
+      if constexpr (G16) mma16816(c, pl0, ql1, pl2, ql3, b0, b1);   // low parts of both row groups
+      A.o[m + u][0] = c[0];
+      A.o[m + u][1] = c[1];
+      A.o8[m + u][0] = c[2];
+      A.o8[m + u][1] = c[3];
+    }
   }
 }
 
 // Writes one query head's row: either the normalised bf16 output or the
-// fp32 partial (unnormalised O plus m, l).
+// fp32 partial (unnormalised O plus m, l).  Lane (g, t) holds d = 8m + 2t, +1.
 template <int D>
 CF_DEV void write_row(const float (*o)[2], float m, float l, bool final_out, __nv_bfloat16* out_row,
                       float* part_row, float* ml, int t) {
   if (final_out) {
     const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
-    for (int hh = 0; hh < D / 64; ++hh) {
-      uint4 lo, hi;
-      lo.x = pack_bf16(o[8 * hh + 0][0] * inv, o[8 * hh + 1][0] * inv);
-      lo.y = pack_bf16(o[8 * hh + 2][0] * inv, o[8 * hh + 3][0] * inv);
-      lo.z = pack_bf16(o[8 * hh + 4][0] * inv, o[8 * hh + 5][0] * inv);
-      lo.w = pack_bf16(o[8 * hh + 6][0] * inv, o[8 * hh + 7][0] * inv);
-      hi.x = pack_bf16(o[8 * hh + 0][1] * inv, o[8 * hh + 1][1] * inv);
-      hi.y = pack_bf16(o[8 * hh + 2][1] * inv, o[8 * hh + 3][1] * inv);
-      hi.z = pack_bf16(o[8 * hh + 4][1] * inv, o[8 * hh + 5][1] * inv);
-      hi.w = pack_bf16(o[8 * hh + 6][1] * inv, o[8 * hh + 7][1] * inv);
-      uint4* dst = reinterpret_cast<uint4*>(out_row + 64 * hh + 16 * t);
-      dst[0] = lo;
-      dst[1] = hi;
-    }
+    for (int k = 0; k < D / 8; ++k)
+      *reinterpret_cast<uint32_t*>(out_row + 8 * k + 2 * t) = pack_bf16(o[k][0] * inv, o[k][1] * inv);
   } else {
 #pragma unroll
-    for (int hh = 0; hh < D / 64; ++hh) {
-      float4* dst = reinterpret_cast<float4*>(part_row + 64 * hh + 16 * t);
-      dst[0] = make_float4(o[8 * hh + 0][0], o[8 * hh + 1][0], o[8 * hh + 2][0], o[8 * hh + 3][0]);
-      dst[1] = make_float4(o[8 * hh + 4][0], o[8 * hh + 5][0], o[8 * hh + 6][0], o[8 * hh + 7][0]);
-      dst[2] = make_float4(o[8 * hh + 0][1], o[8 * hh + 1][1], o[8 * hh + 2][1], o[8 * hh + 3][1]);
-      dst[3] = make_float4(o[8 * hh + 4][1], o[8 * hh + 5][1], o[8 * hh + 6][1], o[8 * hh + 7][1]);
-    }
+    for (int k = 0; k < D / 8; ++k)
+      *reinterpret_cast<float2*>(part_row + 8 * k + 2 * t) = make_float2(o[k][0], o[k][1]);
     if (t == 0) {
       ml[0] = m;
       ml[1] = l;
@@ -302,19 +298,48 @@ CF_DEV int build_plan(const DecodeArgs& a, int* s_pref, int* s_pages) {
   return s_chunk;
 }
 
-template <int D, bool G16>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
-  extern __shared__ int dsm[];
-  int* s_pref = dsm;              // [n + 1]
-  int* s_pages = dsm + a.n + 1;   // [n]
-  const int chunk = build_plan(a, s_pref, s_pages);
-  const int G = a.Hq / a.Hkv;
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const long long total = (long long)s_pref[a.n] * a.Hkv;
-  const int nwarps = gridDim.x * kDecodeWarps;
-  const int gw = blockIdx.x * kDecodeWarps + (threadIdx.x >> 5);
 
-  for (long long item = gw; item < total; item += nwarps) {
+template <int D, bool G16>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, DecodeArgs a) {
+  using R = Ring<D>;
+  extern __shared__ __align__(16) uint8_t dsm_raw[];
+  int* dsm;
+  {
+    const uint32_t s0 = smem_u32(dsm_raw);
+    dsm = reinterpret_cast<int*>(dsm_raw + (((s0 + 1023u) & ~1023u) - s0));
+  }
+  int* s_pref = dsm;                          // [n + 1]
+  int* s_pages = dsm + kMaxDecodeReqs + 1;    // [n]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(dsm) + kPlanBytes + kRingBytes);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecodeWarps * R::STAGES; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  const int chunk = build_plan(a, s_pref, s_pages);   // ends with __syncthreads
+  uint64_t* full = bars + warp * R::STAGES;
+  const uint32_t ring = smem_u32(dsm) + kPlanBytes + warp * R::STAGES * R::PAGE;
+  const int G = a.Hq / a.Hkv;
+  const int g = lane >> 2, t = lane & 3;
+  const long long total = (long long)s_pref[a.n] * a.Hkv;
+  const int oob_row = a.num_pages * a.Hkv * 16;   // first row past the pool: zero-filled box
+  volatile int no_abort = 0;
+  const WaitCtl wc{&no_abort, a.err, a.wait_ns};
+
+  if (total > a.max_items) {   // cannot happen with the plan bound; never write past the partials
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, CF_DEVERR_CONTEXT);
+    return;
+  }
+  uint32_t issued = 0, consumed = 0;   // pages of this warp, over all its items
+  bool ok_run = true;
+  // items are taken from a global queue: (request, chunk, KV head), head fastest
+  int item = 0;
+  if (lane == 0) item = atomicAdd(a.counter, 1);
+  item = __shfl_sync(0xffffffffu, item, 0);
+  while (item < total && ok_run) {
     const int cg = (int)(item / a.Hkv), h = (int)(item % a.Hkv);
     int lo = 0, hi = a.n;  // largest j with s_pref[j] <= cg
     while (hi - lo > 1) {
@@ -329,17 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     const int p0 = c * chunk, p1 = min(pages, p0 + chunk);
     const int* table = a.pages + (size_t)j * a.page_stride;
 
-    // Q fragments of rows g (head h*G + g) and g + 8
+    // Q fragments (natural d order): k-step s uses d = 16 s + 2 t (+8)
     uint32_t qa[D / 16][2], qb[G16 ? D / 16 : 1][2];
     const __nv_bfloat16* qrow = a.q + (size_t)j * a.q_stride + (size_t)h * G * D;
 #pragma unroll
-    for (int jj = 0; jj < D / 32; ++jj) {
-      const uint4 v = g < G ? *reinterpret_cast<const uint4*>(qrow + g * D + (4 * jj + t) * 8) : make_uint4(0, 0, 0, 0);
-      qa[2 * jj][0] = v.x; qa[2 * jj][1] = v.y; qa[2 * jj + 1][0] = v.z; qa[2 * jj + 1][1] = v.w;
+    for (int st = 0; st < D / 16; ++st) {
+      qa[st][0] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + g * D + 16 * st + 2 * t) : 0u;
+      qa[st][1] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + g * D + 16 * st + 8 + 2 * t) : 0u;
       if constexpr (G16) {
-        const uint4 u = g + 8 < G ? *reinterpret_cast<const uint4*>(qrow + (g + 8) * D + (4 * jj + t) * 8)
-                                  : make_uint4(0, 0, 0, 0);
-        qb[2 * jj][0] = u.x; qb[2 * jj][1] = u.y; qb[2 * jj + 1][0] = u.z; qb[2 * jj + 1][1] = u.w;
+        qb[st][0] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qrow + (g + 8) * D + 16 * st + 2 * t) : 0u;
+        qb[st][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qrow + (g + 8) * D + 16 * st + 8 + 2 * t) : 0u;
       }
     }
     Acc<D, G16> A;
@@ -351,22 +375,73 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     A.m0 = A.m1 = -INFINITY;
     A.l0 = A.l1 = 0.f;
 
-    PageRegs<D> ra, rb;
-    if (p0 < p1) load_page<D>(ra, a, table, p0, keys - 0, h, g, t);
-    for (int p = p0; p < p1; p += 2) {
-      if (p + 1 < p1) load_page<D>(rb, a, table, p + 1, keys, h, g, t);
-      process_page<D, G16>(A, ra, qa, qb, a.scale_log2, t);
-      if (p + 1 >= p1) break;
-      if (p + 2 < p1) load_page<D>(ra, a, table, p + 2, keys, h, g, t);
-      process_page<D, G16>(A, rb, qa, qb, a.scale_log2, t);
+    // ring pipeline: up to STAGES pages in flight; lane 0 issues the TMA
+    // copies of page p0 + k into slot (issued % STAGES)
+    const int np = p1 - p0;
+    uint32_t okmask = 0;   // bit s: the page in ring slot s has a valid id
+    int k_issue = 0;
+    for (; k_issue < np && k_issue < R::STAGES; ++k_issue) {
+      const int sl = issued % R::STAGES;
+      const int pid = table[p0 + k_issue];
+      const bool ok = pid >= 0 && pid < a.num_pages;
+      okmask = ok ? (okmask | (1u << sl)) : (okmask & ~(1u << sl));
+      if (lane == 0) {
+        const int row = ok ? (pid * a.Hkv + h) * 16 : oob_row;
+        const uint32_t kt = ring + sl * R::PAGE;
+        mbar_expect_tx(&full[sl], R::PAGE);
+#pragma unroll
+        for (int hd = 0; hd < D / 64; ++hd) {
+          tma_load_2d_u32(kt + hd * R::HALF, &tmK, &full[sl], hd * 64, row);
+          tma_load_2d_u32(kt + R::KV + hd * R::HALF, &tmV, &full[sl], hd * 64, row);
+        }
+      }
+      ++issued;
     }
+    int pid_next = k_issue < np ? table[p0 + k_issue] : -1;
+    for (int i = 0; i < np; ++i) {
+      const int sl = consumed % R::STAGES;
+      if (!mbar_wait(&full[sl], (consumed / R::STAGES) & 1, wc)) {
+        ok_run = false;
+        break;
+      }
+      const int p = p0 + i;
+      int valid = keys - p * 16;
+      valid = valid > 16 ? 16 : valid;
+      if (!((okmask >> sl) & 1u)) {
+        if (lane == 0) set_error(a.err, CF_DEVERR_PAGE);
+        valid = 0;
+      }
+      const uint32_t kt = ring + sl * R::PAGE;
+      process_page<D, G16>(A, kt, kt + R::KV, valid, qa, qb, a.scale_log2, lane);
+      ++consumed;
+      __syncwarp();   // every lane has read the slot before it is refilled
+      if (k_issue < np) {
+        const int sl2 = issued % R::STAGES;
+        const bool ok = pid_next >= 0 && pid_next < a.num_pages;
+        okmask = ok ? (okmask | (1u << sl2)) : (okmask & ~(1u << sl2));
+        if (lane == 0) {
+          fence_proxy_async_smem();   // the slot's generic-proxy reads come before the TMA refill
+          const int row = ok ? (pid_next * a.Hkv + h) * 16 : oob_row;
+          const uint32_t kt2 = ring + sl2 * R::PAGE;
+          mbar_expect_tx(&full[sl2], R::PAGE);
+#pragma unroll
+          for (int hd = 0; hd < D / 64; ++hd) {
+            tma_load_2d_u32(kt2 + hd * R::HALF, &tmK, &full[sl2], hd * 64, row);
+            tma_load_2d_u32(kt2 + R::KV + hd * R::HALF, &tmV, &full[sl2], hd * 64, row);
+          }
+        }
+        ++issued;
+        ++k_issue;
+        pid_next = k_issue < np ? table[p0 + k_issue] : -1;
+      }
+    }
+    if (!ok_run) break;
     A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 1);
     A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 2);
     if constexpr (G16) {
       A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 1);
       A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 2);
-    }
-    if constexpr (!G16) {
+    } else {
 #pragma unroll
       for (int m = 0; m < D / 8; ++m) {
         A.o[m][0] += A.o8[m][0];
@@ -389,15 +464,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         write_row<D>(A.o8, A.m1, A.l1, final_out, orow, prow, ml, t);
       }
     }
+    if (lane == 0) item = atomicAdd(a.counter, 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
+  }
+  if (!ok_run) {   // a wait gave up: let this warp's own copies land before exiting
+    volatile int dummy = 0;
+    const WaitCtl w2{&dummy, nullptr, a.wait_ns};
+    while (consumed < issued) {
+      mbar_wait(&full[consumed % R::STAGES], (consumed / R::STAGES) & 1, w2);
+      ++consumed;
+    }
   }
 }
-
 // One warp per (request, query head): merges the chunk partials.
 template <int D>
 __global__ void decode_merge_kernel(DecodeArgs a) {
   const int G = a.Hq / a.Hkv;
   const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.counter = 0;   // the decode kernel has finished with it
   if (w >= (long long)a.n * a.Hq) return;
   const int j = (int)(w / a.Hq), hq = (int)(w % a.Hq);
   const int h = hq / G, g = hq % G;
@@ -436,7 +521,7 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
 }
 
 template <int D, bool G16>
-cudaError_t launch_t(const DecodeArgs& a, int ctas, cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int ctas, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -444,7 +529,7 @@ cudaError_t launch_t(const DecodeArgs& a, int ctas, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  decode_kernel<D, G16><<<ctas, kThreads, kDecodeSmem, s>>>(a);
+  decode_kernel<D, G16><<<ctas, kThreads, kDecodeSmem, s>>>(tk, tv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = (long long)a.n * a.Hq;
@@ -459,12 +544,15 @@ long long decode_max_items(int max_decode, int Hkv, int max_ctas) {
   return (long long)kItemsPerWarp * max_ctas * kDecodeWarps + (long long)max_decode * Hkv + 64;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int num_ctas, cudaStream_t s) {
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int num_ctas,
+                          cudaStream_t s) {
   if (a.n <= 0) return cudaSuccess;
-  if ((a.n * 2 + 2) * 4 > kDecodeSmem) return cudaErrorInvalidValue;
+  if (a.n > kMaxDecodeReqs) return cudaErrorInvalidValue;
   const bool g16 = a.Hq / a.Hkv > 8;
-  if (a.head_dim == 128) return g16 ? launch_t<128, true>(a, num_ctas, s) : launch_t<128, false>(a, num_ctas, s);
-  if (a.head_dim == 64) return g16 ? launch_t<64, true>(a, num_ctas, s) : launch_t<64, false>(a, num_ctas, s);
+  if (a.head_dim == 128)
+    return g16 ? launch_t<128, true>(tk, tv, a, num_ctas, s) : launch_t<128, false>(tk, tv, a, num_ctas, s);
+  if (a.head_dim == 64)
+    return g16 ? launch_t<64, true>(tk, tv, a, num_ctas, s) : launch_t<64, false>(tk, tv, a, num_ctas, s);
   return cudaErrorInvalidValue;
 }
 

@@ -74,7 +74,10 @@ extern "C" cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int h
   int ctas = num_sms > 0 ? num_sms : sms;
   if (ctas > sms) ctas = sms;
 
-  // Scratch layout: error word | chunk plan | (m, l) partials | O partials.
+  // Scratch layout: error word (byte 0) and work-queue counter (byte 128) |
+  // chunk plan | (m, l) partials | O partials.  The counter must be 0 when a
+  // call starts: it is 0 when the library is loaded and the merge kernel of
+  // every call sets it back to 0.
   const int G = n_q_heads / n_kv_heads;
   const long long items = decode_max_items(n, n_kv_heads, ctas);
   const size_t off_plan = 256;
@@ -83,6 +86,12 @@ extern "C" cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int h
   const size_t need = off_o + (size_t)items * G * head_dim * 4;
   if (need > kScratchBytes) return CF_ERR_INVALID_ARG;   // batch too large for the static scratch
 
+  const uint64_t rows = (uint64_t)pool->num_pages * n_kv_heads * page_size;
+  if (rows >= (1ull << 31)) return CF_ERR_UNSUPPORTED;
+  CUtensorMap tk, tv;
+  if (!make_tmap_2d(&tk, pool->k, rows, head_dim, head_dim, 16, 64) ||
+      !make_tmap_2d(&tv, pool->v, rows, head_dim, head_dim, 16, 64))
+    return CF_ERR_CUDA;
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return CF_ERR_CUDA;
   uint8_t* b = static_cast<uint8_t*>(base);
@@ -105,9 +114,11 @@ extern "C" cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int h
   da.page_size = page_size;
   da.scale_log2 = (float)(1.4426950408889634 / sqrt((double)head_dim));
   da.err = reinterpret_cast<int*>(b);
+  da.counter = reinterpret_cast<int*>(b + 128);
   da.plan = reinterpret_cast<int*>(b + off_plan);
   da.part_ml = reinterpret_cast<float*>(b + off_ml);
   da.part_o = reinterpret_cast<float*>(b + off_o);
   da.max_items = items;
-  return launch_decode(da, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+  da.wait_ns = 2000000000ull;
+  return launch_decode(tk, tv, da, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }

@@ -124,6 +124,7 @@ struct cf_engine {
   float *part_o, *part_ml;
   int* plan;
   int* counter;
+  int* dec_counter;
   int* err;
   long long max_items;
   Tmaps tm;
@@ -138,6 +139,7 @@ struct cf_engine {
   long long ring_next = 0;
   double phase_ms[kPhases] = {0};
   int phase_steps = 0;
+  std::vector<std::pair<int, float>> calib;   // (decode CTAs, ms) of the last calibration
 };
 
 namespace {
@@ -171,7 +173,7 @@ cf_status check_config(const cf_config* c) {
   if (c->page_size != kPageSize) return CF_ERR_UNSUPPORTED;
   if (c->hidden % 256 || qkv_dim(*c) % 256 || c->ffn_dim % 128 || (c->n_q_heads * c->head_dim) % 64)
     return CF_ERR_UNSUPPORTED;
-  if (c->max_decode > 4096) return CF_ERR_UNSUPPORTED;
+  if (c->max_decode > 2048) return CF_ERR_UNSUPPORTED;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return CF_ERR_INVALID_ARG;
   return CF_OK;
 }
@@ -354,6 +356,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   const size_t o_cs = take(T * (d / 2) * 8), o_slot = take(T * 4), o_inv = take(d / 2 * 8);
   const size_t o_po = take((size_t)e->max_items * G * d * 4), o_pml = take((size_t)e->max_items * G * 2 * 4);
   const size_t o_plan = take((size_t)(c.max_decode + 4) * 4), o_cnt = take(4), o_err = take(4);
+  const size_t o_dcnt = take(4);
   e->ws_bytes = off;
   if (cudaMalloc(&e->ws, off) != cudaSuccess) {
     cudaGetLastError();
@@ -375,6 +378,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   e->plan = reinterpret_cast<int*>(b + o_plan);
   e->counter = reinterpret_cast<int*>(b + o_cnt);
   e->err = reinterpret_cast<int*>(b + o_err);
+  e->dec_counter = reinterpret_cast<int*>(b + o_dcnt);
   bool ok = cudaMemset(e->ws, 0, off) == cudaSuccess;
   // RoPE inverse frequencies theta^(-2i/d), in double
   std::vector<double> inv(d / 2);
@@ -483,8 +487,11 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     da.part_ml = e->part_ml;
     da.plan = e->plan;
     da.max_items = e->max_items;
+    da.counter = e->dec_counter;
+    da.wait_ns = kWaitNs;
+  da.wait_ns = kWaitNs;
     da.err = e->err;
-    CF_CUDA(e, launch_decode(da, n_dec_sms, e->dstream));
+    CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, n_dec_sms, e->dstream));
     e->launches += 2;
     if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], e->dstream));
     CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
@@ -605,6 +612,8 @@ cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride, co
     return fail(e, CF_ERR_INVALID_ARG, "row stride shorter than Hq * d");
   cf_status st = check_pool(e, pool);
   if (st != CF_OK) return st;
+  st = pool_maps(e, pool);
+  if (st != CF_OK) return st;
   int ctas = num_sms > 0 ? num_sms : e->sms;
   if (ctas > e->sms) ctas = e->sms;
   DecodeArgs da{};
@@ -629,8 +638,10 @@ cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride, co
   da.part_ml = e->part_ml;
   da.plan = e->plan;
   da.max_items = e->max_items;
+  da.counter = e->dec_counter;
+  da.wait_ns = kWaitNs;
   da.err = e->err;
-  CF_CUDA(e, launch_decode(da, ctas, static_cast<cudaStream_t>(stream)));
+  CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, ctas, static_cast<cudaStream_t>(stream)));
   e->launches += 2;
   return CF_OK;
 }
@@ -775,6 +786,101 @@ cf_status cf_set_decode_sms(cf_engine* e, int n) {
   if (!e || n < 0 || n >= e->sms) return CF_ERR_INVALID_ARG;
   e->decode_sms = n;
   return CF_OK;
+}
+
+cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* bt, const cf_kv_pool* pool, float frac,
+                                  void* stream, int* chosen) {
+  if (!e || !bt || !chosen || !(frac > 0.f && frac <= 1.f)) return fail(e, CF_ERR_INVALID_ARG, "bad argument");
+  cf_status st = check_batch(e, bt);
+  if (st != CF_OK) return st;
+  if (bt->n_decode == 0) return fail(e, CF_ERR_INVALID_ARG, "no decode requests to calibrate on");
+  st = check_pool(e, pool);
+  if (st != CF_OK) return st;
+  st = pool_maps(e, pool);
+  if (st != CF_OK) return st;
+  const cf_config& c = e->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t row = (size_t)c.n_q_heads * c.head_dim;
+  DecodeArgs da{};
+  da.q = e->q + (size_t)bt->prefill_len * row;   // Q rows of the last step's decodes
+  da.q_stride = (long long)row;
+  da.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
+  da.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
+  da.num_pages = pool->num_pages;
+  da.n = bt->n_decode;
+  da.n_keys = bt->dec_ctx;
+  da.key_offset = 1;
+  da.pages = bt->dec_pages;
+  da.page_stride = bt->dec_stride;
+  da.out = e->attn + (size_t)bt->prefill_len * row;
+  da.out_stride = (long long)row;
+  da.Hq = c.n_q_heads;
+  da.Hkv = c.n_kv_heads;
+  da.head_dim = c.head_dim;
+  da.page_size = c.page_size;
+  da.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+  da.part_o = e->part_o;
+  da.part_ml = e->part_ml;
+  da.plan = e->plan;
+  da.max_items = e->max_items;
+  da.counter = e->dec_counter;
+  da.wait_ns = kWaitNs;
+  da.err = e->err;
+  cudaEvent_t t0, t1;
+  CF_CUDA(e, cudaEventCreate(&t0));
+  CF_CUDA(e, cudaEventCreate(&t1));
+  std::vector<std::pair<int, float>> res;
+  for (int n = 4; n <= e->sms; n += (n < 16 ? 4 : 8)) {
+    const int ctas = n > e->sms ? e->sms : n;
+    for (int w = 0; w < 2; ++w) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, ctas, s));
+    CF_CUDA(e, cudaEventRecord(t0, s));
+    for (int r = 0; r < 5; ++r) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, ctas, s));
+    CF_CUDA(e, cudaEventRecord(t1, s));
+    CF_CUDA(e, cudaEventSynchronize(t1));
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, t0, t1);
+    res.push_back({ctas, ms / 5});
+    e->launches += 14;
+  }
+  {  // all SMs
+    for (int w = 0; w < 2; ++w) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, e->sms, s));
+    CF_CUDA(e, cudaEventRecord(t0, s));
+    for (int r = 0; r < 5; ++r) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, e->sms, s));
+    CF_CUDA(e, cudaEventRecord(t1, s));
+    CF_CUDA(e, cudaEventSynchronize(t1));
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, t0, t1);
+    res.push_back({e->sms, ms / 5});
+    e->launches += 14;
+  }
+  cudaEventDestroy(t0);
+  cudaEventDestroy(t1);
+  float best = 1e30f;
+  for (auto& r : res) best = r.second < best ? r.second : best;
+  int pick = e->sms - 1;
+  for (auto& r : res)
+    if (best / r.second >= frac) {
+      pick = r.first;
+      break;
+    }
+  if (pick >= e->sms) pick = e->sms - 1;
+  e->decode_sms = pick;
+  e->calib.assign(res.begin(), res.end());
+  *chosen = pick;
+  return CF_OK;
+}
+
+int cf_calibration_points(cf_engine* e, int* sms, float* ms, int cap) {
+  if (!e) return 0;
+  int n = 0;
+  for (auto& r : e->calib) {
+    if (n < cap) {
+      sms[n] = r.first;
+      ms[n] = r.second;
+    }
+    ++n;
+  }
+  return n;
 }
 
 cf_status cf_set_profiling(cf_engine* e, int on) {

@@ -105,11 +105,15 @@ struct DecodeArgs {
   float* part_ml;                 // [max_items][G][2] (max in log2 units, sum)
   int* plan;                      // [n + 2]: chunk prefix sums, chunk pages
   long long max_items;
+  int* counter;                   // work-queue counter; 0 at launch, reset to 0 by the merge kernel
   int* err;
+  unsigned long long wait_ns;     // cap of one mbarrier wait
 };
 constexpr int kDecodeWarps = 8;
 long long decode_max_items(int max_decode, int Hkv, int max_ctas);
-cudaError_t launch_decode(const DecodeArgs& a, int num_ctas, cudaStream_t s);
+// tmK/tmV: 2-D {d, pages*Hkv*ps} maps over the pools, box {64, 16}, 128-byte swizzle
+cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a, int num_ctas,
+                          cudaStream_t s);
 
 // ------------------------------------------------------------------ prefill attention
 struct PrefillArgs {

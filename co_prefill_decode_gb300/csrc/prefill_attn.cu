@@ -284,15 +284,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&s_free[sb]);
         ++sc;
         const int kv0 = j * BKV;
-        const bool masked = kv0 + BKV - 1 > diag;
-        float mx = -INFINITY;
+        if (kv0 + BKV - 1 > diag) {   // tile crosses the diagonal or the end of the request
 #pragma unroll
-        for (int c = 0; c < BKV; ++c) {
-          const int kp = kv0 + c;
-          const bool vis = !masked || (kp <= qpos && kp < kend);
-          s[c] = vis ? s[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < BKV; ++c) {
+            const int kp = kv0 + c;
+            if (!(kp <= qpos && kp < kend)) s[c] = -INFINITY;
+          }
         }
+        // row max with 8 independent partial maxima (short dependency chains)
+        float mp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mp[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < BKV; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * a.scale_log2;
         // wait until PV_{j-1} is done: O may be rescaled and P rewritten
         if (j > 0) {
           if (!mbar_wait(pv_done, (pc & 1), wc)) { ok = false; break; }
@@ -319,14 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        float ls = 0.f;
+        const float sc2 = a.scale_log2;
+        float lp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) lp[i] = 0.f;
 #pragma unroll
         for (int c8 = 0; c8 < BKV / 8; ++c8) {
           float p[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            p[i] = fast_exp2(s[c8 * 8 + i] - mu);
-            ls += p[i];
+            p[i] = fast_exp2(fmaf(s[c8 * 8 + i], sc2, -mu));
+            lp[i] += p[i];
           }
           uint4 w;
           w.x = pack_bf16(p[0], p[1]);
@@ -336,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int half = c8 >> 3, ch = c8 & 7;
           *reinterpret_cast<uint4*>(p_tile + half * C::HALF + r * 128 + ((ch ^ (r & 7)) << 4)) = w;
         }
+        const float ls = ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
         l += ls;
         // keys past the end of the request: zero their V rows (slots may hold anything)
         const int vst = vc & 1;

@@ -68,7 +68,7 @@ typedef struct {
     float rms_eps;       /* RMSNorm epsilon (also used by QK-norm)               */
     int qk_norm;         /* 1: per-head RMSNorm of q and k over d before RoPE    */
     int max_tokens;      /* largest T = l + n_decode of any step                 */
-    int max_decode;      /* largest n_decode of any step                         */
+    int max_decode;      /* largest n_decode of any step (<= 2048)               */
     int decode_sms;      /* SMs given to decode attention in the fork; 0 = auto  */
 } cf_config;
 
@@ -251,6 +251,17 @@ void* cf_engine_buffer(cf_engine* e, const char* name);
 int cf_engine_decode_sms(cf_engine* e);
 cf_status cf_set_decode_sms(cf_engine* e, int n);
 cf_status cf_set_profiling(cf_engine* e, int on);
+/* The decode SM share by the ConfluxServe §6.1 rule: "the minimum number of
+ * SMs needed to sustain 90% of its standalone peak HBM bandwidth".  Times the
+ * decode attention of batch b (on the Q rows the engine's last cf_layer_step
+ * produced, over `pool`) alone at increasing CTA counts, picks the smallest
+ * count whose time is within 1/frac of the fastest, stores it as the
+ * engine's decode share and returns it in *chosen.  Synchronous; overwrites
+ * the engine's attention buffer.  cf_calibration_points copies the measured
+ * (CTAs, ms) pairs (returns how many there are). */
+cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* b, const cf_kv_pool* pool, float frac,
+                                  void* stream, int* chosen);
+int cf_calibration_points(cf_engine* e, int* sms, float* ms, int cap);
 cf_status cf_get_phase_times(cf_engine* e, float* ms, int n, int* steps);
 long long cf_launch_count(cf_engine* e);
 
