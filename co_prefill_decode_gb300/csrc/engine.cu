@@ -757,6 +757,7 @@ cf_status cf_get_error(cf_engine* e, char* buf, int len) {
     if (word & CF_DEVERR_PAGE) msg += " page id outside the pool;";
     if (word & CF_DEVERR_CONTEXT) msg += " context longer than its page table;";
     if (word & CF_DEVERR_TIMEOUT) msg += " bounded wait expired;";
+    if (word & CF_DEVERR_INTERNAL) msg += " kernel refused to run (internal check);";
     st = (word & CF_DEVERR_TIMEOUT) ? CF_ERR_TIMEOUT : CF_ERR_DEVICE;
   } else if (!e->last_error.empty()) {
     msg = e->last_error;

@@ -53,6 +53,7 @@ typedef enum {
 #define CF_DEVERR_PAGE     0x1   /* a page id outside [0, num_pages) was skipped */
 #define CF_DEVERR_CONTEXT  0x2   /* a context needs more pages than its table has */
 #define CF_DEVERR_TIMEOUT  0x4   /* a bounded mbarrier wait gave up              */
+#define CF_DEVERR_INTERNAL 0x8   /* a kernel refused to run (e.g. misaligned shared memory) */
 
 typedef struct cf_engine cf_engine;
 

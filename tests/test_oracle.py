@@ -385,3 +385,4 @@ def test_oracle_chain_sensitivity(monkeypatch):
     got = L.layer_step(x, W, w.shape, b, kp, vp)
     e = np.abs(got["out"] - ref["out"]) / np.maximum(1.0, np.abs(ref["out"]))
     assert 2e-3 < e.max() < 0.1 and e.mean() < 1e-2
+
