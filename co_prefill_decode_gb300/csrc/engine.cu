@@ -123,7 +123,7 @@ struct cf_engine {
   double* inv_freq;
   float *part_o, *part_ml;
   int* plan;
-  int* counter;
+  unsigned* counter;             // prefill work queue (set to 0 before each use)
   int* dec_counter;
   int* err;
   long long max_items;
@@ -247,6 +247,7 @@ cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const void* x, const CUten
   pa.num_pages = pool->num_pages;
   pa.page_size = c.page_size;
   pa.err = e->err;
+  pa.zero = e->counter;   // the prefill work queue of this step starts at 0
   CF_CUDA(e, launch_prep(pa, s));
   e->launches++;
   if (ev_mid) CF_CUDA(e, cudaEventRecord(ev_mid, s));
@@ -376,7 +377,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   e->part_o = reinterpret_cast<float*>(b + o_po);
   e->part_ml = reinterpret_cast<float*>(b + o_pml);
   e->plan = reinterpret_cast<int*>(b + o_plan);
-  e->counter = reinterpret_cast<int*>(b + o_cnt);
+  e->counter = reinterpret_cast<unsigned*>(b + o_cnt);
   e->err = reinterpret_cast<int*>(b + o_err);
   e->dec_counter = reinterpret_cast<int*>(b + o_dcnt);
   bool ok = cudaMemset(e->ws, 0, off) == cudaSuccess;
@@ -494,7 +495,6 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, n_dec_sms, e->dstream));
     e->launches += 2;
     if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], e->dstream));
-    CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
   }
   if (l > 0) {
     if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE0], s));
@@ -510,14 +510,25 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     pf.out = e->attn;
     pf.out_stride = (long long)Hq * d;
     pf.scale_log2 = scale_log2;
-    pf.counter = e->counter;
+    pf.counter = e->counter;   // zeroed by this step's prep kernel
+    pf.base = 0;
     pf.err = e->err;
     pf.wait_ns = kWaitNs;
     CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_pre_sms, s));
     e->launches++;
+    if (nd > 0) {
+      // Work-conserving split: once decode has finished, a second prefill
+      // grid on the decode stream takes the SMs it leaves and drains the same
+      // work queue.  Decode still owns its SMs for as long as it runs.
+      CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_dec_sms, e->dstream));
+      e->launches++;
+    }
     if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE1], s));
   }
-  if (nd > 0) CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_join, 0));
+  if (nd > 0) {
+    CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
+    CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_join, 0));
+  }
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_JOIN], s));
 
   // a6: O-proj + residual -> h (fp32)
@@ -676,6 +687,8 @@ cf_status cf_prefill_attn(cf_engine* e, const void* q, const cf_kv_pool* pool, i
   pf.out_stride = (long long)c.n_q_heads * c.head_dim;
   pf.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
   pf.counter = e->counter;
+  pf.base = 0;
+  CF_CUDA(e, cudaMemsetAsync(e->counter, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream)));
   pf.err = e->err;
   pf.wait_ns = kWaitNs;
   CF_CUDA(e, launch_prefill(tq, e->pm.tk, e->pm.tv, pf, ctas, static_cast<cudaStream_t>(stream)));

@@ -78,6 +78,7 @@ struct PrepArgs {
   const int* pre_pages;
   int num_pages, page_size;
   int* err;
+  unsigned* zero;                 // if set, block 0 stores 0 here (resets a work queue)
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
@@ -123,10 +124,14 @@ struct PrefillArgs {
   __nv_bfloat16* out;             // row i at out + i * out_stride, [Hq][d]
   long long out_stride;
   float scale_log2;
-  int* counter;                   // work queue counter (zeroed before launch)
+  unsigned* counter;              // work queue shared by the launches of one step
+  unsigned base;                  // counter value at the start of this launch's queue (0)
   int* err;
   unsigned long long wait_ns;
 };
+// CTAs a launch really uses (<= items), and the items of a launch.
+int prefill_grid(const PrefillArgs& a, int num_ctas);
+int prefill_items(const PrefillArgs& a);
 // tmQ: 3-D {d, Hq, rows} over q with box {64, 1, 128};
 // tmK/tmV: 2-D {d, pages*Hkv*ps} over the pools with box {64, 16}.
 cudaError_t launch_prefill(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,

@@ -59,7 +59,7 @@ struct PfCfg {
   static constexpr uint32_t OFF_X = OFF_V + KV_STAGES * KV_BYTES;   // row exchange [NSPLIT][128] fp32
   static constexpr uint32_t OFF_BAR = OFF_X + Split<D>::NSPLIT * 128 * 4;
   // no alignment slack: the kernel checks that the base is 1 KB aligned
-  static constexpr size_t SMEM = OFF_BAR + 256;
+  static constexpr size_t SMEM = OFF_BAR + 512;   // mbarriers, item ring, TMEM address
   static_assert(SMEM <= 232448, "shared memory per CTA");
   // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256 + D), P0 [384, 448), P1 [448, 512)
   // (P holds 128 bf16 keys per row, two per 32-bit column)
@@ -108,7 +108,9 @@ __global__ void __launch_bounds__(Split<D>::THREADS, 1)
   uint64_t* pv_done = p_full + 2;          // [2]
   uint64_t* o_free = pv_done + 2;
   uint64_t* drain = o_free + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* item_ready = drain + 1;        // [8] per item-ring slot
+  volatile int* ring = reinterpret_cast<volatile int*>(item_ready + 8);   // [8] item ids
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(Split<D>::THREADS, 1)
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(o_free, Split<D>::SOFTMAX_THREADS);
+    for (int i = 0; i < 8; ++i) mbar_init(&item_ready[i], 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -167,21 +170,40 @@ __global__ void __launch_bounds__(Split<D>::THREADS, 1)
     bool ok = true;
     uint32_t last_q = 0xffffffffu, last_k[NS], last_v[NS];
     for (int i = 0; i < NS; ++i) last_k[i] = last_v[i] = 0xffffffffu;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-      const Item it = item_of(idx, a.Hq, n_qt);
-      const int kvh = it.head / G;
-      if (lane == 0 && !is_v) {
-        ok = mbar_wait(q_empty, (qc & 1) ^ 1, wc);
-        if (ok) {
-          mbar_expect_tx(q_full, C::Q_BYTES);
+    for (int k = 0; ok; ++k) {
+      // Work items come from a queue shared by every CTA of this launch and
+      // of a second launch that picks up the SMs decode leaves behind.  Warp
+      // 0 takes the next item once the Q buffer is free and publishes it to
+      // the other warps through an 8-slot ring (no warp is more than 4 items
+      // behind the fetcher, so a slot is always read before it is reused).
+      int idx = -1;
+      if (!is_v) {
+        if (lane == 0) {
+          ok = mbar_wait(q_empty, (qc & 1) ^ 1, wc);
+          if (ok) {
+            const unsigned got = atomicAdd(a.counter, 1u) - a.base;
+            idx = got < (unsigned)n_items ? (int)got : -1;
+            ring[k & 7] = idx;
+            mbar_arrive(&item_ready[k & 7]);
+            if (idx >= 0) {
+              const Item it0 = item_of(idx, a.Hq, n_qt);
+              mbar_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
-          for (int hd = 0; hd < D / 64; ++hd)
-            tma_load_3d(smem + C::OFF_Q + hd * C::HALF, &tmQ, q_full, hd * 64, it.head, it.qt * BQ);
-          last_q = qc & 1;
+              for (int hd = 0; hd < D / 64; ++hd)
+                tma_load_3d(smem + C::OFF_Q + hd * C::HALF, &tmQ, q_full, hd * 64, it0.head, it0.qt * BQ);
+              last_q = qc & 1;
+            }
+          }
         }
+      } else if (lane == 0) {
+        ok = mbar_wait(&item_ready[k & 7], (k >> 3) & 1, wc);
+        idx = ok ? ring[k & 7] : -1;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (!ok || idx < 0) break;
+      const Item it = item_of(idx, a.Hq, n_qt);
+      const int kvh = it.head / G;
       ++qc;
       const int nkv = kv_tiles(a, it.qt);
       int pid = (lane < 8 && lane < n_pages_req) ? a.pages[lane] : -1;
@@ -246,7 +268,10 @@ __global__ void __launch_bounds__(Split<D>::THREADS, 1)
       const uint64_t qdesc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
       int qc = 0, kc = 0, sc = 0, pc = 0, oc = 0;
       bool ok = true, issued = false;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      for (int k = 0; ok; ++k) {
+        if (!mbar_wait(&item_ready[k & 7], (k >> 3) & 1, wc)) { ok = false; break; }
+        const int idx = ring[k & 7];
+        if (idx < 0) break;
         const Item it = item_of(idx, a.Hq, n_qt);
         const int nkv = kv_tiles(a, it.qt);
         if (!mbar_wait(q_full, qc & 1, wc)) { ok = false; break; }
@@ -335,7 +360,11 @@ __global__ void __launch_bounds__(Split<D>::THREADS, 1)
       row_sync();
       return t;
     };
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (int k = 0; ok; ++k) {
+      if (!mbar_wait(&item_ready[k & 7], (k >> 3) & 1, wc)) ok = false;
+      const int idx = ok ? ring[k & 7] : -1;
+      // every thread of a row reads the same slot: they leave together
+      if (idx < 0) break;
       const Item it = item_of(idx, a.Hq, n_qt);
       const int nkv = kv_tiles(a, it.qt);
       const int qi = it.qt * BQ + r;
@@ -495,14 +524,20 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int n_items = ((a.l + BQ - 1) / BQ) * a.Hq;
-  if (ctas > n_items) ctas = n_items;
-  if (ctas < 1) ctas = 1;
+  ctas = prefill_grid(a, ctas);
   prefill_kernel<D><<<ctas, Split<D>::THREADS, PfCfg<D>::SMEM, s>>>(q, k, v, a);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int prefill_grid(const PrefillArgs& a, int ctas) {
+  const int n_items = ((a.l + BQ - 1) / BQ) * a.Hq;
+  if (ctas > n_items) ctas = n_items;
+  return ctas < 1 ? 1 : ctas;
+}
+
+int prefill_items(const PrefillArgs& a) { return ((a.l + BQ - 1) / BQ) * a.Hq; }
 
 cudaError_t launch_prefill(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const PrefillArgs& a, int num_ctas, cudaStream_t s) {

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
   const int row = blockIdx.x;
   const int H = a.H;
   __shared__ float red[kPrepThreads / 32];
+  if (a.zero && row == 0 && threadIdx.x == 0) *a.zero = 0u;
   if (a.xn != nullptr) {
   float ss = 0.f;
   // vectorised: 8 elements per step
