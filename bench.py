@@ -33,9 +33,7 @@ METRIC = "co-batched layer step µs & tokens/s; decode attn % HBM peak; GEMM % B
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture of the same shape; set to None whenever that kernel changes.
-DOMINANT_TRAFFIC = {
-    "l8b": {"bytes": 243647488 + 21766912, "source": "profiles/gemm_gateup_l8b_T1040.md"},
-}
+DOMINANT_TRAFFIC = {}   # workload -> {"bytes": DRAM bytes per launch, "source": ncu summary}; empty until re-captured
 
 
 def load_peaks():

@@ -28,7 +28,7 @@ EXPORTS = (
     "cf_prefill_attn", "cf_gemm", "cf_kv_append", "cf_get_error", "cf_engine_buffer",
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
-    "cf_calibration_points",
+    "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k",
 )
 
 
@@ -94,6 +94,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_calibration_points": (I, [P, ctypes.POINTER(I), ctypes.POINTER(F), I]),
         "cf_decode_attn_noalloc": (I, [I, I, I, I, P, L, ctypes.POINTER(cf_kv_pool), I, P, P, I, P, L, I, P]),
         "cf_qkv": (I, [P, ctypes.POINTER(cf_batch), P, ctypes.POINTER(cf_kv_pool), P, P]),
+        "cf_gemm_schedule": (I, [I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
+                                 ctypes.POINTER(I)]),
+        "cf_set_split_k": (I, [P, I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -128,6 +131,16 @@ def _check(lib, eng, status: int):
 
 def device_sm_count() -> int:
     return int(load_library().cf_device_sm_count())
+
+
+def cf_gemm_schedule(M: int, N: int, K: int, epilogue: int = CF_EPI_NONE, ctas: int = 152,
+                     split_mode: int = 0) -> dict:
+    """Work split of a GEMM on `ctas` persistent CTAs (host only)."""
+    lib = load_library()
+    g, t, d, sp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib, None, lib.cf_gemm_schedule(M, N, K, epilogue, ctas, split_mode, ctypes.byref(g),
+                                           ctypes.byref(t), ctypes.byref(d), ctypes.byref(sp)))
+    return {"grid": g.value, "tiles": t.value, "dp_tiles": d.value, "split": sp.value}
 
 
 def make_config(shape, max_tokens: int, max_decode: int, decode_sms: int = 0, page_size: int = 16) -> cf_config:
@@ -228,6 +241,10 @@ class Engine:
 
     def cf_set_decode_sms(self, n: int):
         _check(self.lib, self.handle, self.lib.cf_set_decode_sms(self.handle, n))
+
+    def cf_set_split_k(self, mode: int):
+        """0: automatic, 1: whole tiles only (batch-invariant rows), n >= 2: n k-chunks."""
+        _check(self.lib, self.handle, self.lib.cf_set_split_k(self.handle, int(mode)))
 
     def cf_set_profiling(self, on: bool):
         _check(self.lib, self.handle, self.lib.cf_set_profiling(self.handle, int(on)))

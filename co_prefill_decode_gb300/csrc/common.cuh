@@ -95,6 +95,17 @@ CF_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+// Untiled bulk copy global -> shared (16-byte aligned, bytes % 16 == 0),
+// completing `bytes` of transaction count on `bar`.
+CF_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+// Orders this thread's generic-proxy view of global memory before its later
+// async-proxy (bulk copy) accesses.
+CF_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 CF_DEV void tma_load_2d_u32(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(

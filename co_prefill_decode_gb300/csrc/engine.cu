@@ -125,6 +125,9 @@ struct cf_engine {
   int* plan;
   unsigned* counter;             // prefill work queue (set to 0 before each use)
   int* dec_counter;
+  int split_mode = 0;            // GEMM split-K tail: 0 automatic, 1 off, >= 2 forced chunk count
+  float* sk_ws;                  // split-K partial tiles of the GEMMs
+  int* sk_flags;                 // their per-tile flags (0 between launches)
   int* err;
   long long max_items;
   Tmaps tm;
@@ -272,6 +275,9 @@ cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const void* x, const CUten
   g.qkv.q_out = static_cast<__nv_bfloat16*>(q_out);
   g.qkv.k_pool = static_cast<__nv_bfloat16*>(pool->k);
   g.qkv.v_pool = static_cast<__nv_bfloat16*>(pool->v);
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
   CF_CUDA(e, launch_gemm(tm_xn, e->tm.wqkv, e->tm.wqkv, g, e->sms, s));
   e->launches++;
   return CF_OK;
@@ -358,6 +364,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   const size_t o_po = take((size_t)e->max_items * G * d * 4), o_pml = take((size_t)e->max_items * G * 2 * 4);
   const size_t o_plan = take((size_t)(c.max_decode + 4) * 4), o_cnt = take(4), o_err = take(4);
   const size_t o_dcnt = take(4);
+  const size_t o_skw = take(gemm_sk_ws_bytes(e->sms)), o_skf = take(gemm_sk_flag_bytes(e->sms));
   e->ws_bytes = off;
   if (cudaMalloc(&e->ws, off) != cudaSuccess) {
     cudaGetLastError();
@@ -380,6 +387,8 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   e->counter = reinterpret_cast<unsigned*>(b + o_cnt);
   e->err = reinterpret_cast<int*>(b + o_err);
   e->dec_counter = reinterpret_cast<int*>(b + o_dcnt);
+  e->sk_ws = reinterpret_cast<float*>(b + o_skw);
+  e->sk_flags = reinterpret_cast<int*>(b + o_skf);
   bool ok = cudaMemset(e->ws, 0, off) == cudaSuccess;
   // RoPE inverse frequencies theta^(-2i/d), in double
   std::vector<double> inv(d / 2);
@@ -543,6 +552,9 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   g.ld_aux = H;
   g.err = e->err;
   g.wait_ns = kWaitNs;
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
   CF_CUDA(e, launch_gemm(e->tm.attn, e->tm.wo, e->tm.wo, g, e->sms, s));
   e->launches++;
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_OPROJ], s));
@@ -562,6 +574,9 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   g.ldo = F;
   g.err = e->err;
   g.wait_ns = kWaitNs;
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
   CF_CUDA(e, launch_gemm(e->tm.hn, e->tm.wg, e->tm.wu, g, e->sms, s));
   e->launches++;
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_GU], s));
@@ -578,6 +593,9 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   g.ld_aux = H;
   g.err = e->err;
   g.wait_ns = kWaitNs;
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
   CF_CUDA(e, launch_gemm(e->tm.act, e->tm.wd, e->tm.wd, g, e->sms, s));
   e->launches++;
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_END], s));
@@ -732,8 +750,30 @@ cf_status cf_gemm(cf_engine* e, const void* A, int lda, const void* B, int ldb, 
     case CF_EPI_RESID_BF16: g.epi = EPI_RESID_BF16; g.aux = aux; g.ld_aux = ldc; break;
     case CF_EPI_SWIGLU: g.epi = EPI_SWIGLU; break;
   }
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
   CF_CUDA(e, launch_gemm(ta, tb0, tb1, g, e->sms, static_cast<cudaStream_t>(stream)));
   e->launches++;
+  return CF_OK;
+}
+
+cf_status cf_gemm_schedule(int M, int N, int K, int epilogue, int ctas, int split_mode, int* grid, int* tiles,
+                           int* dp_tiles, int* split) {
+  if (M <= 0 || N <= 0 || K <= 0 || ctas <= 0 || split_mode < 0) return CF_ERR_INVALID_ARG;
+  if (epilogue < CF_EPI_NONE || epilogue > CF_EPI_SWIGLU) return CF_ERR_INVALID_ARG;
+  const GemmSchedule sc =
+      gemm_schedule(M, N, K, epilogue == CF_EPI_SWIGLU ? EPI_SWIGLU : EPI_BF16, ctas, split_mode);
+  if (grid) *grid = sc.grid;
+  if (tiles) *tiles = sc.tiles;
+  if (dp_tiles) *dp_tiles = sc.dp_tiles;
+  if (split) *split = sc.split;
+  return CF_OK;
+}
+
+cf_status cf_set_split_k(cf_engine* e, int split_mode) {
+  if (!e || split_mode < 0) return CF_ERR_INVALID_ARG;
+  e->split_mode = split_mode;
   return CF_OK;
 }
 
@@ -760,6 +800,8 @@ cf_status cf_get_error(cf_engine* e, char* buf, int len) {
   int word = 0;
   if (r == cudaSuccess) r = cudaMemcpy(&word, e->err, 4, cudaMemcpyDeviceToHost);
   if (r == cudaSuccess && word) r = cudaMemset(e->err, 0, 4);
+  // a launch that gave up may leave split-K tile flags set: clear them
+  if (r == cudaSuccess && word) r = cudaMemset(e->sk_flags, 0, gemm_sk_flag_bytes(e->sms));
   std::string msg;
   cf_status st = CF_OK;
   if (r != cudaSuccess) {

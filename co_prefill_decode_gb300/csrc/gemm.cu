@@ -9,6 +9,18 @@
 // [prefill; decode] token matrix is the A operand, so every weight tile is
 // fetched once for both phases (ConfluxServe §4 "Cross-SP co-batch", App. B
 // Table 7: weight traffic amortised over all co-batched tokens).
+//
+// Work is dealt by a fixed schedule (gemm_schedule): every CTA takes whole
+// tiles, one per wave, for all full waves.  When the tiles of the last wave
+// would leave many SMs idle, each of them is cut into S equal k-chunks and
+// the chunks are dealt chunk-major, one per CTA, so CTAs running at the same
+// time read the same k range of the shared weight tiles.  A cut tile is
+// finished by the CTA running its last chunk: the others store their fp32
+// partial accumulators to a workspace; since the chunk is that CTA's final
+// unit its TMA ring is idle by then, so it pulls the partials into the ring
+// with bulk copies, adds them in k order followed by its own (a fixed order,
+// so results are deterministic), puts the sum back into TMEM and applies the
+// epilogue as for a whole tile.
 #include <stdio.h>
 
 #include "common.cuh"
@@ -38,6 +50,144 @@ CF_DEV uint8_t* align1024(uint8_t* p) {
 }
 
 CF_DEV float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+// One unit of work: k-blocks [kb0, kb1) of tile `tile` (m-fastest numbering).
+struct Unit {
+  int tile, kb0, kb1;
+};
+
+// The units of CTA `c` in order: whole tiles c, c + G, ... below dp_tiles,
+// then (if c < (tiles - dp_tiles) * split) chunk c / R of tail tile
+// dp_tiles + c % R, R = tiles - dp_tiles; chunk s covers k-blocks
+// [s * num_kb / split, (s + 1) * num_kb / split).
+struct UnitIter {
+  int c, G, num_kb, dp_tiles, tail, split;
+  int j;
+  bool tail_done;
+  CF_DEV UnitIter(int c_, int G_, int num_kb_, int tiles, int dp_tiles_, int split_)
+      : c(c_), G(G_), num_kb(num_kb_), dp_tiles(dp_tiles_), tail(tiles - dp_tiles_), split(split_), j(0),
+        tail_done(false) {}
+  CF_DEV bool next(Unit& u) {
+    const int tile = c + j * G;
+    if (tile < dp_tiles) {
+      u = Unit{tile, 0, num_kb};
+      ++j;
+      return true;
+    }
+    if (tail_done || c >= tail * split) return false;
+    tail_done = true;
+    const int s = c / tail;
+    u = Unit{dp_tiles + c % tail, s * num_kb / split, (s + 1) * num_kb / split};
+    return true;
+  }
+};
+
+CF_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Split-K fix-up of a tail unit (a k-chunk of a cut tile).  Returns 1 when
+// this CTA holds the tile's full sum in TMEM and must run the epilogue, 0
+// when it handed its partial over, -1 when the wait for the other chunks
+// gave up (error word set).  `ring` is the CTA's TMA stage memory, idle once
+// the last unit's accumulator is full.
+template <int BN>
+CF_DEV int sk_fixup(uint32_t taddr, int r_in_tile, int ep_tid, const Unit& u, const GemmArgs& p, uint8_t* ring,
+                    uint32_t ring_bytes, uint64_t* fix_bar, volatile int* sh_flag, const WaitCtl& wc) {
+  const int tail = p.tiles - p.dp_tiles;
+  const int it = u.tile - p.dp_tiles;   // tail tile index; its chunk s is run by CTA s * tail + it
+  const int S = p.split;
+  const int s_me = blockIdx.x / tail;
+  int* flag = p.sk_flags + it;          // partials stored so far
+  // Partial layout: float4 j (columns 4j..4j+3) of tile row r at
+  // slot + j * BM + r, so the rows of a warp fill 512 contiguous bytes per
+  // access, and the 32 columns c..c+31 form one contiguous 16 KB piece.
+  constexpr uint32_t kPiece = BM * 32 * 4;
+  constexpr size_t kSlot4 = (size_t)BM * BN / 4;
+  float4* ws4 = reinterpret_cast<float4*>(p.sk_ws);
+  float v[32];
+  if (s_me < S - 1) {  // store the partial, then count it
+    float4* dst = ws4 + (size_t)blockIdx.x * kSlot4 + r_in_tile;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      tmem_ld32(taddr + c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        __stcg(dst + (size_t)(c / 4 + i) * BM, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+    }
+    __threadfence();
+    epi_bar();
+    if (ep_tid == 0) atomicAdd(flag, 1);
+    return 0;
+  }
+  // the last chunk: wait until the other S - 1 partials are stored
+  if (ep_tid == 0) {
+    const uint64_t t_start = globaltimer();
+    int ok = 1;
+    while (*reinterpret_cast<volatile int*>(flag) < S - 1) {
+      if (*wc.abort) {
+        ok = 0;
+        break;
+      }
+      if (globaltimer() - t_start > wc.limit_ns) {
+        *wc.abort = 1;
+        set_error(wc.err, CF_DEVERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    *sh_flag = ok;
+    __threadfence();
+    fence_proxy_async_global();
+  }
+  epi_bar();
+  if (!*sh_flag) return -1;
+  // rounds of whole 32-column chunks: all S - 1 pieces of a chunk per round
+  const int per_round = (int)(ring_bytes / kPiece) / (S - 1);
+  const float4* ring4 = reinterpret_cast<const float4*>(ring);
+  int round = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN / 32 && ok; c0 += per_round, ++round) {
+    const int nc = BN / 32 - c0 < per_round ? BN / 32 - c0 : per_round;
+    if (ep_tid == 0) {
+      mbar_expect_tx(fix_bar, (uint32_t)(nc * (S - 1)) * kPiece);
+      for (int c = 0; c < nc; ++c)
+        for (int j = 0; j < S - 1; ++j)
+          bulk_load(ring + (size_t)(c * (S - 1) + j) * kPiece,
+                    ws4 + (size_t)(j * tail + it) * kSlot4 + (size_t)(c0 + c) * (kPiece / 16), kPiece, fix_bar);
+    }
+    ok = mbar_wait(fix_bar, round & 1, wc);
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < nc; ++c) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        for (int j = 0; j < S - 1; ++j) {   // chunks in k order ...
+          const float4* src = ring4 + (size_t)(c * (S - 1) + j) * (kPiece / 16) + r_in_tile;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 q = src[i * BM];
+            v[4 * i] += q.x;
+            v[4 * i + 1] += q.y;
+            v[4 * i + 2] += q.z;
+            v[4 * i + 3] += q.w;
+          }
+        }
+        float own[32];   // ... then this CTA's own, the last in k
+        tmem_ld32(taddr + (c0 + c) * 32, own);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += own[i];
+        tmem_st32(taddr + (c0 + c) * 32, v);
+      }
+    }
+    epi_bar();   // the ring is read before the next round overwrites it
+  }
+  tmem_st_wait();
+  if (ep_tid == 0) *flag = 0;   // free for the next launch
+  return ok ? 1 : -1;
+}
 
 CF_DEV void store_bf16x32(__nv_bfloat16* dst, const float* v) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -133,8 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* fix_bar = drain + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fix_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* sh_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -147,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[a], 128);
     }
     mbar_init(drain, 1);
+    mbar_init(fix_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -166,8 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
   const int num_m = (p.M + BM - 1) / BM;
-  const int num_n = EPI == EPI_SWIGLU ? p.N / (BN / 2) : p.N / BN;
-  const int num_tiles = num_m * num_n;
   const int num_kb = p.K / BK;
 
   if (warp == 0) {
@@ -177,11 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t last_phase[8];
       for (int s = 0; s < 8; ++s) last_phase[s] = 0xffffffffu;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int mt = tile % num_m, nt = tile / num_m;
+      UnitIter ui(blockIdx.x, gridDim.x, num_kb, p.tiles, p.dp_tiles, p.split);
+      Unit u;
+      while (ok && ui.next(u)) {
+        const int mt = u.tile % num_m, nt = u.tile / num_m;
         const int brow0 = EPI == EPI_SWIGLU ? nt * (BN / 2) : nt * BN;
         const int brow1 = EPI == EPI_SWIGLU ? brow0 : brow0 + BN / 2;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
             ok = false;
             break;
@@ -215,13 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true, issued = false;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+      UnitIter ui(blockIdx.x, gridDim.x, num_kb, p.tiles, p.dp_tiles, p.split);
+      Unit u;
+      for (; ok && ui.next(u); ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, wc)) {
             ok = false;
             break;
@@ -233,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b0 + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb != u.kb0) | (k != 0));
           }
           issued = true;
           umma_commit(&empty[stage]);
@@ -254,16 +409,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {  // ---------------- epilogue warps 2..5
     const int quarter = warp & 3;
     const int r_in_tile = quarter * 32 + lane;
+    const int ep_tid = threadIdx.x - 64;
     int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    UnitIter ui(blockIdx.x, gridDim.x, num_kb, p.tiles, p.dp_tiles, p.split);
+    Unit u;
+    for (; ui.next(u); ++it) {
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
       tc_fence_after();
-      const int mt = tile % num_m, nt = tile / num_m;
+      const int mt = u.tile % num_m, nt = u.tile / num_m;
       const int row = mt * BM + r_in_tile;
       const bool valid = row < p.M;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if (u.kb0 != 0 || u.kb1 != num_kb) {
+        const int own = sk_fixup<BN>(taddr, r_in_tile, ep_tid, u, p, smem, STAGES * C::STAGE_BYTES, fix_bar,
+                                     sh_flag, wc);
+        if (own <= 0) {
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          if (own < 0) break;
+          continue;
+        }
+      }
       float v[32], w[32];
       if constexpr (EPI == EPI_BF16) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * BN;
@@ -363,22 +531,71 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int num_m = (p.M + BM - 1) / BM;
-  const int num_n = EPI == EPI_SWIGLU ? p.N / (BN / 2) : p.N / BN;
-  int grid = num_m * num_n;
-  int cap = p.max_ctas > 0 ? p.max_ctas : num_sms;
-  if (grid > cap) grid = cap;
-  if (grid < 1) grid = 1;
-  k<<<grid, kThreads, C::SMEM, s>>>(a, b0, b1, p);
+  const int cap = p.max_ctas > 0 && p.max_ctas < num_sms ? p.max_ctas : num_sms;
+  GemmArgs q = p;
+  const GemmSchedule sc = gemm_schedule(p.M, p.N, p.K, EPI, cap, (q.sk_ws && q.sk_flags) ? p.split_mode : 1);
+  q.tiles = sc.tiles;
+  q.dp_tiles = sc.dp_tiles;
+  q.split = sc.split;
+  k<<<sc.grid, kThreads, C::SMEM, s>>>(a, b0, b1, q);
   return cudaGetLastError();
 }
+
+// Critical-path cost of the split-K fix-up, in k-blocks (one k-block of a
+// 128x256 tile is ~0.3 us on an SM): storing a partial and signalling it,
+// then per extra chunk a 128 KB bulk read back, measured as ~9 us in all.
+constexpr int kFixupBaseKb = 30;
+constexpr int kFixupPerChunkKb = 4;
+// at most 12 partial pieces of a 32-column chunk fit the fix-up's ring rounds
+constexpr int kMaxSplit = 13;
 
 }  // namespace
 
 int gemm_block_n(int epi) {
   (void)epi;
-  return 256;
+  return kGemmBN;
 }
+
+// split_mode: 0 automatic, 1 whole tiles only, >= 2 that many k-chunks per
+// tail tile (at most what fits in one wave).
+GemmSchedule gemm_schedule(int M, int N, int K, int epi, int ctas, int split_mode) {
+  if (ctas < 1) ctas = 1;
+  GemmSchedule sc{};
+  const int num_m = (M + BM - 1) / BM;
+  const int num_n = epi == EPI_SWIGLU ? N / (kGemmBN / 2) : N / kGemmBN;
+  sc.tiles = num_m * num_n;
+  sc.num_kb = K / BK;
+  sc.dp_tiles = sc.tiles;
+  sc.split = 1;
+  sc.grid = sc.tiles < ctas ? sc.tiles : ctas;
+  if (sc.grid < 1) sc.grid = 1;
+  const int rest = sc.tiles % ctas;
+  if (split_mode == 1 || rest == 0 || sc.tiles <= 0) return sc;
+  int max_split = ctas / rest < sc.num_kb ? ctas / rest : sc.num_kb;
+  if (max_split > kMaxSplit) max_split = kMaxSplit;
+  if (max_split < 2) return sc;
+  int best = 1;
+  if (split_mode >= 2) {
+    best = split_mode < max_split ? split_mode : max_split;
+  } else {
+    long long best_t = sc.num_kb;   // the tail as one more wave of whole tiles
+    for (int s = 2; s <= max_split; ++s) {
+      const long long t = (sc.num_kb + s - 1) / s + kFixupBaseKb + (long long)kFixupPerChunkKb * (s - 1);
+      if (t < best_t) {
+        best_t = t;
+        best = s;
+      }
+    }
+  }
+  if (best < 2) return sc;
+  sc.dp_tiles = sc.tiles - rest;
+  sc.split = best;
+  sc.grid = sc.dp_tiles > 0 ? ctas : rest * best;
+  return sc;
+}
+
+size_t gemm_sk_ws_bytes(int ctas) { return (size_t)ctas * BM * kGemmBN * sizeof(float); }
+size_t gemm_sk_flag_bytes(int ctas) { return (size_t)ctas * sizeof(int); }
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB0, const CUtensorMap& tmB1,
                         const GemmArgs& a, int num_sms, cudaStream_t s) {

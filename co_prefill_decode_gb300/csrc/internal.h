@@ -41,7 +41,24 @@ struct GemmArgs {
   int* err;
   unsigned long long wait_ns;
   int max_ctas;                   // persistent grid cap (0 = all SMs)
+  // split-K tail of the last wave (tiles .. split set by launch_gemm from gemm_schedule)
+  int split_mode;                 // 0 automatic, 1 whole tiles only, >= 2 forced chunk count
+  float* sk_ws;                   // [grid][BM * BN] fp32 partial tiles, one slot per CTA
+  int* sk_flags;                  // [tail tiles]: partials stored; 0 between launches
+  int tiles, dp_tiles, split;     // tiles [dp_tiles, tiles) are cut into `split` k-chunks
 };
+
+// Persistent schedule of one GEMM on `ctas` CTAs: whole BMxBN tiles for the
+// full waves; the tiles of a partial last wave are cut into `split` k-chunks
+// when that shortens the critical path.
+struct GemmSchedule {
+  int grid, tiles, num_kb, dp_tiles, split;
+};
+GemmSchedule gemm_schedule(int M, int N, int K, int epi, int ctas, int split_mode);
+constexpr int kGemmBN = 256;
+// bytes of sk_ws / sk_flags a GEMM needs on up to `ctas` CTAs
+size_t gemm_sk_ws_bytes(int ctas);
+size_t gemm_sk_flag_bytes(int ctas);
 
 // Builds a 2-D bf16 TMA descriptor with 128-byte swizzle: rows x cols
 // (cols contiguous, row stride `ld` elements), box = box_rows x 64.

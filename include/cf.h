@@ -199,6 +199,28 @@ cf_status cf_gemm(cf_engine* e, const void* A, int lda, const void* B, int ldb,
                   void* C, int ldc, int M, int N, int K, int epilogue,
                   const void* aux, void* stream);
 
+/* Work split of a GEMM over `ctas` persistent CTAs, as cf_gemm and the
+ * layer step's GEMMs use it (host only; needs no GPU).  Tiles are 128 x 256
+ * outputs (128 x 128 of the result for SwiGLU), numbered m-fastest; K is cut
+ * into 64-wide k-blocks.  Tiles [0, *dp_tiles) fill whole waves, one tile
+ * per CTA per wave.  The *tiles - *dp_tiles tiles of a partial last wave are
+ * each cut into *split equal k-chunks (1: not cut), run one chunk per CTA,
+ * so the last wave does not leave SMs idle; a cut tile is summed in k order
+ * by the CTA that finishes last, so results are deterministic.  split_mode:
+ * 0 chooses the cut from a cost model, 1 never cuts, n >= 2 cuts into n
+ * chunks (at most what fits in one wave).  A row's rounding depends on
+ * whether its tile was cut, i.e. on M: with split_mode 1 every output row is
+ * bit-identical however many other rows share the batch (ConfluxServe §4:
+ * co-batched rows are independent).  Returns CF_ERR_INVALID_ARG for
+ * non-positive sizes or ctas. */
+cf_status cf_gemm_schedule(int M, int N, int K, int epilogue, int ctas, int split_mode, int* grid, int* tiles,
+                           int* dp_tiles, int* split);
+
+/* Split-K mode of this engine's GEMMs (see cf_gemm_schedule); default 0.
+ * With 1 the GEMM rows of a layer step are bit-identical to the same rows
+ * run in any other batch. */
+cf_status cf_set_split_k(cf_engine* e, int split_mode);
+
 /* Decode attention that allocates nothing.  The paper has no counterpart:
  * this entry point exists for callers that cannot allocate device memory --
  * a serving runtime whose own pool already holds all free device memory, a

@@ -30,26 +30,40 @@ def int_bf16(shape, seed, lo=-4, hi=4):
 
 # --------------------------------------------------------------------- GEMM
 @pytest.mark.parametrize("M,N,K", [(1, 256, 64), (68, 512, 256), (200, 768, 4096), (1040, 512, 1024),
-                                   (300, 256, 8192), (1040, 6144, 512), (4128, 2048, 256)])
+                                   (300, 256, 8192), (1040, 6144, 512), (4128, 2048, 256),
+                                   (384, 4096, 14336), (1040, 6144, 4096)])
 def test_gemm_exact_integers(cf, M, N, K):
     """Small integers: fp32 accumulation is exact, so the GPU equals the integer
     product bit for bit (fp32 out via the residual epilogue with zero aux) and
-    its bf16 rounding (plain epilogue)."""
+    its bf16 rounding (plain epilogue).  Shapes whose last wave is partial
+    cut those tiles into k-chunks (see cf_gemm_schedule), also with every
+    forced chunk count tried here: a k-block lost or added in the cut shows
+    up here."""
     eng = engine_for(cf, wl.TINY)
     A, B = int_bf16((M, K), 1), int_bf16((N, K), 2)
     exact = f64(A) @ f64(B).T
     C32 = torch.empty(M, N, dtype=torch.float32, device="cuda")
-    eng.cf_gemm(A, B, C32, cf.CF_EPI_RESID_F32, aux=torch.zeros(M, N, dtype=torch.bfloat16, device="cuda"))
-    C16 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    eng.cf_gemm(A, B, C16, cf.CF_EPI_NONE)
-    torch.cuda.synchronize()
-    assert np.array_equal(f64(C32), exact)
-    assert np.array_equal(f64(C16), oracle.bf16_round(exact))
+    z = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    for mode in (0, 1, 2, 7):
+        eng.cf_set_split_k(mode)
+        C32.fill_(float("nan"))
+        eng.cf_gemm(A, B, C32, cf.CF_EPI_RESID_F32, aux=z)
+        C16 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        eng.cf_gemm(A, B, C16, cf.CF_EPI_NONE)
+        torch.cuda.synchronize()
+        assert np.array_equal(f64(C32), exact), mode
+        assert np.array_equal(f64(C16), oracle.bf16_round(exact)), mode
+    eng.cf_set_split_k(0)
+    assert eng.cf_get_error()[0] == 0
 
 
-def test_gemm_epilogues(cf):
+@pytest.mark.parametrize("K", [1024, 8192])
+def test_gemm_epilogues(cf, K):
+    """Every epilogue against fp64; K = 8192 cuts each of the 6 tiles into
+    k-chunks, so the split-K fix-up feeds every epilogue."""
     eng = engine_for(cf, wl.TINY)
-    M, N, K = 333, 512, 1024
+    M, N = 333, 512
+    assert (cf.cf_gemm_schedule(M, N, K)["split"] > 1) == (K == 8192)
     A, B = randn_bf16((M, K), 3), randn_bf16((N, K), 4, std=0.03)
     U = randn_bf16((N, K), 5, std=0.03)
     res16 = randn_bf16((M, N), 6)
@@ -62,7 +76,8 @@ def test_gemm_epilogues(cf):
     o3 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     eng.cf_gemm(A, B, o3, cf.CF_EPI_SWIGLU, aux=U)
     torch.cuda.synchronize()
-    assert_close(out, f64(res16) + a @ b.T, "resid f32", 1e-5, 1e-6)
+    # fp32 accumulation: the rounding error of a K-term dot product grows with K
+    assert_close(out, f64(res16) + a @ b.T, "resid f32", 1e-5 * K / 1024, 1e-6 * K / 1024)
     assert_close(o2, oracle.bf16_round(f64(res32) + a @ b.T), "resid bf16")
     assert_close(o3, oracle.bf16_round(oracle.swiglu(a @ b.T, a @ u.T)), "swiglu")
 
@@ -82,17 +97,52 @@ def test_gemm_swiglu_many_tiles(cf):
 
 
 def test_gemm_rows_are_independent(cf):
-    """Co-batching invariance (ConfluxServe §4): a row of the stacked GEMM is
-    bit-identical to the same row computed in a smaller batch."""
+    """Co-batching invariance (ConfluxServe §4): with split-K off a row of
+    the stacked GEMM is bit-identical to the same row computed in a smaller
+    batch; with it on, tiles are cut into k-chunks depending on the batch,
+    so the rows agree within fp32 accumulation rounding."""
     eng = engine_for(cf, wl.TINY)
     K, N = 2048, 768
+    assert cf.cf_gemm_schedule(700, N, K, split_mode=4)["split"] == 4
     A, B = randn_bf16((700, K), 8), randn_bf16((N, K), 9, std=0.02)
     full = torch.empty(700, N, dtype=torch.bfloat16, device="cuda")
     part = torch.empty(130, N, dtype=torch.bfloat16, device="cuda")
+    full32 = torch.empty(700, N, dtype=torch.float32, device="cuda")
+    part32 = torch.empty(130, N, dtype=torch.float32, device="cuda")
+    z = torch.zeros(700, N, dtype=torch.bfloat16, device="cuda")
+    a = A[500:630].contiguous()
+    eng.cf_set_split_k(4)   # the full batch's tiles cut in 4 k-chunks ...
+    eng.cf_gemm(A, B, full32, cf.CF_EPI_RESID_F32, aux=z)
+    eng.cf_set_split_k(1)   # ... the small batch's tiles whole
+    eng.cf_gemm(a, B, part32, cf.CF_EPI_RESID_F32, aux=z[:130])
     eng.cf_gemm(A, B, full)
-    eng.cf_gemm(A[500:630].contiguous(), B, part)
+    eng.cf_gemm(a, B, part)
+    eng.cf_set_split_k(0)
     torch.cuda.synchronize()
     assert torch.equal(full[500:630], part)
+    d = (full32[500:630] - part32).abs().max().item()
+    assert d <= 1e-5 * max(1.0, part32.abs().max().item())
+
+
+def test_gemm_stream_k_is_deterministic(cf):
+    """Chunks of a cut tile are summed in k order by whichever CTA finishes
+    last, so repeated calls agree bit for bit (the 48-tile, 224-k-block FFN
+    down projection of a 384-token batch)."""
+    eng = engine_for(cf, wl.TINY)
+    M, N, K = 384, 4096, 14336
+    assert cf.cf_gemm_schedule(M, N, K, cf.CF_EPI_RESID_BF16)["split"] > 1
+    A, B = randn_bf16((M, K), 11), randn_bf16((N, K), 12, std=0.02)
+    res = torch.randn(M, N, generator=torch.Generator().manual_seed(13)).cuda()
+    outs = []
+    for _ in range(3):
+        o = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        eng.cf_gemm(A, B, o, cf.CF_EPI_RESID_BF16, aux=res)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert eng.cf_get_error()[0] == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = oracle.bf16_round(f64(res) + f64(A) @ f64(B).T)
+    assert_close(outs[0], ref, "stream-K down projection")
 
 
 def test_gemm_rejects_bad_shapes(cf):

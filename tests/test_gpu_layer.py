@@ -285,22 +285,29 @@ def test_layer_page_permutation_invariance(cf):
 
 def test_layer_cobatched_rows_match_separate_batches(cf):
     """ConfluxServe §4: rows of the co-batched step equal the same rows run
-    as a prefill-only and a decode-only step over the same cache.  Prefill
-    rows are bit-identical (GEMM rows are independent, attention items do not
-    depend on the grid); decode rows may split the keys differently, so they
-    agree within fp32 rounding."""
+    as a prefill-only and a decode-only step over the same cache.  With the
+    GEMMs' split-K tail off, prefill rows are bit-identical (GEMM rows are
+    independent, attention items do not depend on the grid); decode rows may
+    split the keys differently, so they agree within fp32 rounding.  With it
+    on, the tile cuts depend on the batch, so prefill rows agree within
+    rounding too."""
     base = wl.WORKLOADS["l8b"]
     dec, l, cp = (300, 64), 96, 40
     S = LayerSetup(wl.reduced(base, dec, l, cp))
-    out = S.step().clone()
     xp, xd = S.x[:l].contiguous(), S.x[l:].contiguous()
-    op, od = torch.empty_like(xp), torch.empty_like(xd)
-    S.eng.cf_layer_step(cf.batch_of(0, None, None, l, cp, S.pre_pages), xp, op, S.pool)
-    S.eng.cf_layer_step(cf.batch_of(len(dec), S.dec_ctx, S.dec_pages, 0, 0, S.pre_pages), xd, od, S.pool)
-    torch.cuda.synchronize()
-    assert S.eng.cf_get_error()[0] == 0
-    assert torch.equal(op, out[:l])
-    assert_close(od, f64(out[l:]), "decode rows", 1e-2, 1e-3)
+    for split_k in (False, True):
+        S.eng.cf_set_split_k(0 if split_k else 1)
+        out = S.step().clone()
+        op, od = torch.empty_like(xp), torch.empty_like(xd)
+        S.eng.cf_layer_step(cf.batch_of(0, None, None, l, cp, S.pre_pages), xp, op, S.pool)
+        S.eng.cf_layer_step(cf.batch_of(len(dec), S.dec_ctx, S.dec_pages, 0, 0, S.pre_pages), xd, od, S.pool)
+        torch.cuda.synchronize()
+        assert S.eng.cf_get_error()[0] == 0
+        if split_k:
+            assert_close(op, f64(out[:l]), "prefill rows", 1e-2, 1e-3)
+        else:
+            assert torch.equal(op, out[:l])
+        assert_close(od, f64(out[l:]), "decode rows", 1e-2, 1e-3)
 
 
 def test_layer_flags_bad_page_id(cf):
