@@ -33,7 +33,11 @@ METRIC = "co-batched layer step µs & tokens/s; decode attn % HBM peak; GEMM % B
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture of the same shape; set to None whenever that kernel changes.
-DOMINANT_TRAFFIC = {}   # workload -> {"bytes": DRAM bytes per launch, "source": ncu summary}; empty until re-captured
+# DRAM bytes (read + write) per launch of the roofline kernel, from one ncu
+# capture of the same kernel build; cleared whenever that kernel changes.
+DOMINANT_TRAFFIC = {
+    "l8b": {"bytes": 243670272 + 21712640, "source": "profiles/gemm_gateup_l8b_T1040.md"},
+}
 
 
 def load_peaks():
