@@ -176,6 +176,9 @@ def s_hidden(w):
 
 
 # ------------------------------------------------------------------ CPU oracle
+REFERENCE_BUDGET_S = 90.0
+
+
 def oracle_sample(w, b, x, weights, kp, vp, rows):
     import numpy as np
     import oracle
@@ -186,10 +189,21 @@ def oracle_sample(w, b, x, weights, kp, vp, rows):
     return time.perf_counter() - t0
 
 
-def reference_rows(b):
-    """Bounded sample for the CPU oracle: the first 64 chunk rows + all decodes."""
-    l = b.prefill_len
-    return list(range(min(64, l))) + list(range(l, l + b.n_decode))
+def reference_rows(b, frac=1.0):
+    """Bounded sample for the CPU oracle: the first 64 chunk rows + all decodes,
+    or the leading fraction `frac` of each (at least 8 chunk rows, 2 decodes)."""
+    l, nd = b.prefill_len, b.n_decode
+    nc = min(l, max(min(8, l), int(round(64 * frac))))
+    ndec = min(nd, max(min(2, nd), int(round(nd * frac))))
+    return list(range(nc)) + list(range(l, l + ndec))
+
+
+def workload_config(w, b, world):
+    """The `config` object both arms report."""
+    return {"workload": f"{w.name}: {w.description}", "tokens_per_step": b.n_tokens, "n_decode": b.n_decode,
+            "prefill_len": b.prefill_len, "prefill_prefix": b.prefill_prefix,
+            "decode_keys": int(sum(int(c) + 1 for c in b.dec_ctx)), "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (weights + KV > 129 MB), no flush"}
 
 
 def blas_threads():
@@ -338,10 +352,7 @@ def run_cf(args, rank, world, local, pg):
         "warmup": args.warmup, "ms_per_step": ms_step, "layer_step_us": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations and KV)",
-        "config": {"workload": f"{w.name}: {w.description}", "tokens_per_step": T, "n_decode": b.n_decode,
-                   "prefill_len": b.prefill_len, "prefill_prefix": b.prefill_prefix,
-                   "decode_keys": wk["decode_keys"], "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (weights + KV > 129 MB), no flush"},
+        "config": workload_config(w, b, world),
         "decode_attn_hbm_frac": (kern["decode_attn"]["gbs"] or 0) / peaks["hbm_gbs"],
         "gemm_bf16_frac": gemm_tflops / peak_tc,
         "prefill_attn_bf16_frac": (kern["prefill_attn"]["tflops"] or 0) / peak_tc,
@@ -357,12 +368,16 @@ def run_cf(args, rank, world, local, pg):
         "peaks": peaks,
     }
     if rank == 0 and not args.no_cpu_baseline:
+        # the oracle as it stands, repeated on its bounded sample for >= 10 s of CPU work
         rows = reference_rows(b)
-        secs = oracle_sample(w, b, x, W, kp, vp, rows)
-        line["cpu_baseline"] = {"value": len(rows) / secs, "unit": "tokens/s", "cores": blas_threads(),
+        secs, reps = 0.0, 0
+        while reps < 3 or (secs < 10.0 and reps < 20):
+            secs += oracle_sample(w, b, x, W, kp, vp, rows)
+            reps += 1
+        line["cpu_baseline"] = {"value": len(rows) * reps / secs, "unit": "tokens/s", "cores": blas_threads(),
                                 "kind": "oracle", "host_cores": os.cpu_count(),
                                 "sample": f"fp64 oracle layer step on {len(rows)} of {T} rows (first 64 chunk rows "
-                                          f"+ all decodes), {secs:.1f} s"}
+                                          f"+ all decodes), {reps} repetitions, {secs:.1f} s"}
     if args.sweep_decode_sms:
         line["decode_sms_sweep"] = sweep_decode_sms(eng, step, args, cf)
     eng.close()
@@ -448,6 +463,9 @@ def run_kernel_case(args):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle timed on the host cores, each step a
+    bounded sample of the workload's rows sized so that all steps take about
+    REFERENCE_BUDGET_S seconds.  Rank 0 only."""
     import workload as wl
     if rank != 0:
         return None
@@ -456,19 +474,23 @@ def run_reference(args, rank, world):
     x = wl.make_x(w, b, args.seed)
     W = wl.make_weights(w, args.seed, unit_gains=True)
     kp, vp = wl.make_pools(w, b, args.seed)
-    rows = reference_rows(b)
-    for _ in range(args.warmup):
-        oracle_sample(w, b, x, W, kp, vp, rows[:8])
+    full = reference_rows(b)
+    t_full = oracle_sample(w, b, x, W, kp, vp, full)            # also the first warm-up step
+    frac = min(1.0, REFERENCE_BUDGET_S / max(1e-6, args.steps * t_full))
+    rows = reference_rows(b, frac)
+    for _ in range(args.warmup - 1):
+        oracle_sample(w, b, x, W, kp, vp, rows)
     secs = [oracle_sample(w, b, x, W, kp, vp, rows) for _ in range(args.steps)]
     total = sum(secs)
     value = len(rows) * args.steps / total
+    sample = (f"fp64 oracle layer step on {len(rows)} of {b.n_tokens} rows per step (leading chunk rows + "
+              f"leading decodes, sized to ~{REFERENCE_BUDGET_S:.0f} s for {args.steps} steps)")
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{w.name}: {w.description}", "rows_per_step": len(rows)},
+            "config": dict(workload_config(w, b, world), rows_per_step=len(rows)),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": f"fp64 oracle on {len(rows)} rows per step (first 64 chunk rows + "
-                                       f"all decodes)"},
+                             "host_cores": os.cpu_count(), "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
