@@ -8,25 +8,28 @@
 // are entirely masked are never visited and only tiles that cross the
 // diagonal are masked.
 //
-// A work item is (128-row query tile, query head).  Persistent CTAs, one per
-// SM of the prefill partition, 6 warps:
-//   warp 0   TMA producer: the Q tile once, then per 128-key tile eight
-//            (page, KV head) boxes of 16 x 64 (x2 for d = 128) for K and for
-//            V (each page is a contiguous 4 KB tile of the pool), one box per
-//            lane, into a 3-stage ring;
+// A work item is (128-row query tile, query head).  Persistent CTAs draw
+// items from a device-wide queue (an atomic counter zeroed earlier in the
+// step), so several grids can share one chunk's items: the layer step runs
+// one grid on the prefill SM partition and, once decode attention is done,
+// a second one on the decode partition.  11 warps per CTA:
+//   warp 0   TMA producer of the Q tile and, per 128-key tile, of the eight
+//            (page, KV head) K boxes of 16 x 64 (x2 for d = 128; each page
+//            is a contiguous 4 KB tile of the pool), one box per lane; lane
+//            0 also takes the next item from the queue and publishes it to
+//            the other roles through a small shared-memory ring;
+//   warp 2   TMA producer of the V boxes, a 3-stage K/V ring in all;
 //   warp 1   one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
 //            buffers, O += P V into a TMEM accumulator;
-//   warps 2+ NSPLIT threads per query row (4 for d = 128), each on 128/NSPLIT
-//            of the tile's keys and 32 of the output columns: load S from
-//            TMEM, combine the row maximum through shared memory (a named
-//            barrier per TMEM lane quarter), online softmax in the log2 domain with
-//            lazy rescaling (O is rescaled in TMEM only when the running max
-//            grows by more than 2^8), write P as bf16 into a 128-byte-swizzled
-//            K-major tile, and at the end normalise O and store it.  Several
-//            softmax warps per SM sub-partition hide each other's latency.
+//   warps 3+ two threads per query row, each on 64 of a tile's keys and
+//            half of the output columns: load S from TMEM, combine the row
+//            maximum and sum through shared memory, online softmax in the
+//            log2 domain with lazy rescaling (O is rescaled in TMEM only
+//            when the running max grows by more than 2^8), write P back to
+//            TMEM as bf16, and at the end normalise O and store it.
 // S_{j+1} is computed while the softmax works on S_j, and PV_j runs while
-// the softmax works on S_{j+1}.  P goes back into TMEM (two buffers) and is
-// the A operand of the PV MMA, which leaves shared memory for three K/V stages.
+// the softmax works on S_{j+1}.  P lives in TMEM (two buffers) and is the A
+// operand of the PV MMA, which leaves shared memory for three K/V stages.
 #include "common.cuh"
 #include "internal.h"
 
