@@ -242,9 +242,10 @@ CF_DEV void write_row(const float (*o)[2], float m, float l, bool final_out, __n
   }
 }
 
-// Chunking plan, computed identically by every CTA from the key counts:
-// pages_j = ceil(keys_j / 16); chunk = max(4, ceil(sum_j pages_j * Hkv /
-// (3 * warps))); chunks_j = ceil(pages_j / chunk); S_j = prefix sums.
+// Chunking plan, computed identically by every CTA of every grid from the
+// key counts: pages_j = ceil(keys_j / 16); chunk = max(4, ceil(sum_j pages_j
+// * Hkv / (4 * warps))) with warps = 8 * plan_ctas; chunks_j =
+// ceil(pages_j / chunk); S_j = prefix sums.
 CF_DEV int build_plan(const DecodeArgs& a, int* s_pref, int* s_pages) {
   const int n = a.n;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
@@ -265,7 +266,7 @@ CF_DEV int build_plan(const DecodeArgs& a, int* s_pref, int* s_pages) {
     for (int j = lane; j < n; j += 32) tot += s_pages[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    const long long warps = (long long)gridDim.x * kDecodeWarps;
+    const long long warps = (long long)a.plan_ctas * kDecodeWarps;
     long long chunk = (tot * a.Hkv + kItemsPerWarp * warps - 1) / (kItemsPerWarp * warps);
     if (chunk < 4) chunk = 4;
     // exclusive prefix sum of chunks_j: lane owns a contiguous block of j
@@ -530,8 +531,11 @@ cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeA
     attr = true;
   }
   decode_kernel<D, G16><<<ctas, kThreads, kDecodeSmem, s>>>(tk, tv, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t merge_t(const DecodeArgs& a, cudaStream_t s) {
   const long long warps = (long long)a.n * a.Hq;
   const int blocks = (int)((warps * 32 + 255) / 256);
   decode_merge_kernel<D><<<blocks, 256, 0, s>>>(a);
@@ -544,16 +548,29 @@ long long decode_max_items(int max_decode, int Hkv, int max_ctas) {
   return (long long)kItemsPerWarp * max_ctas * kDecodeWarps + (long long)max_decode * Hkv + 64;
 }
 
-cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int num_ctas,
-                          cudaStream_t s) {
+cudaError_t launch_decode_kernel(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int num_ctas,
+                                 cudaStream_t s) {
   if (a.n <= 0) return cudaSuccess;
-  if (a.n > kMaxDecodeReqs) return cudaErrorInvalidValue;
+  if (a.n > kMaxDecodeReqs || a.plan_ctas <= 0) return cudaErrorInvalidValue;
   const bool g16 = a.Hq / a.Hkv > 8;
   if (a.head_dim == 128)
     return g16 ? launch_t<128, true>(tk, tv, a, num_ctas, s) : launch_t<128, false>(tk, tv, a, num_ctas, s);
   if (a.head_dim == 64)
     return g16 ? launch_t<64, true>(tk, tv, a, num_ctas, s) : launch_t<64, false>(tk, tv, a, num_ctas, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return cudaSuccess;
+  if (a.head_dim == 128) return merge_t<128>(a, s);
+  if (a.head_dim == 64) return merge_t<64>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int num_ctas,
+                          cudaStream_t s) {
+  cudaError_t e = launch_decode_kernel(tk, tv, a, num_ctas, s);
+  return e == cudaSuccess ? launch_decode_merge(a, s) : e;
 }
 
 }  // namespace cf

@@ -79,7 +79,7 @@ extern "C" cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int h
   // call starts: it is 0 when the library is loaded and the merge kernel of
   // every call sets it back to 0.
   const int G = n_q_heads / n_kv_heads;
-  const long long items = decode_max_items(n, n_kv_heads, ctas);
+  const long long items = decode_max_items(n, n_kv_heads, sms);
   const size_t off_plan = 256;
   const size_t off_ml = align256(off_plan + (size_t)(n + 4) * 4);
   const size_t off_o = align256(off_ml + (size_t)items * G * 2 * 4);
@@ -119,6 +119,7 @@ extern "C" cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int h
   da.part_ml = reinterpret_cast<float*>(b + off_ml);
   da.part_o = reinterpret_cast<float*>(b + off_o);
   da.max_items = items;
+  da.plan_ctas = sms;
   da.wait_ns = 2000000000ull;
   return launch_decode(tk, tv, da, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }

@@ -112,7 +112,7 @@ struct cf_engine {
   int dev = 0, sms = 0;
   int decode_sms = 0;            // 0: auto
   cudaStream_t dstream = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_dec = nullptr;
   // workspace
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -397,6 +397,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   ok = ok && cudaStreamCreateWithFlags(&e->dstream, cudaStreamNonBlocking) == cudaSuccess;
   ok = ok && cudaEventCreateWithFlags(&e->ev_fork, cudaEventDisableTiming) == cudaSuccess;
   ok = ok && cudaEventCreateWithFlags(&e->ev_join, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&e->ev_dec, cudaEventDisableTiming) == cudaSuccess;
   const size_t QKV = qkv_dim(c);
   ok = ok && make_tmap_2d(&e->tm.xn, e->xn, T, H, H, 128, 64);
   ok = ok && make_tmap_2d(&e->tm.attn, e->attn, T, Hq * d, Hq * d, 128, 64);
@@ -424,6 +425,7 @@ void cf_destroy(cf_engine* e) {
   for (cudaEvent_t ev : e->ring) cudaEventDestroy(ev);
   if (e->ev_fork) cudaEventDestroy(e->ev_fork);
   if (e->ev_join) cudaEventDestroy(e->ev_join);
+  if (e->ev_dec) cudaEventDestroy(e->ev_dec);
   if (e->dstream) cudaStreamDestroy(e->dstream);
   if (e->ws) cudaFree(e->ws);
   delete e;
@@ -467,15 +469,18 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   if (st != CF_OK) return st;
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_QKV], s));
 
-  // a3 || a4: the attention fork
+  // a3 || a4: the attention fork.  Decode runs on a second stream with
+  // n_dec_sms CTAs, prefill on `stream` with the rest.  Each kernel drains a
+  // device-wide work queue, so it is work-conserving in both directions:
+  // whichever path finishes first launches a second grid of the other
+  // kernel on its SMs, which takes the remaining items (or none).  Decode's
+  // merge runs once both decode grids are done.
   const int n_dec_sms = pick_decode_sms(e, l > 0, nd > 0);
   const int n_pre_sms = e->sms - n_dec_sms;
   const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+  DecodeArgs da{};
+  PrefillArgs pf{};
   if (nd > 0) {
-    CF_CUDA(e, cudaEventRecord(e->ev_fork, s));
-    CF_CUDA(e, cudaStreamWaitEvent(e->dstream, e->ev_fork, 0));
-    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC0], e->dstream));
-    DecodeArgs da{};
     da.q = e->q + (size_t)l * Hq * d;
     da.q_stride = (long long)Hq * d;
     da.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
@@ -498,16 +503,11 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     da.plan = e->plan;
     da.max_items = e->max_items;
     da.counter = e->dec_counter;
+    da.plan_ctas = e->sms;
     da.wait_ns = kWaitNs;
-  da.wait_ns = kWaitNs;
     da.err = e->err;
-    CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, n_dec_sms, e->dstream));
-    e->launches += 2;
-    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], e->dstream));
   }
   if (l > 0) {
-    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE0], s));
-    PrefillArgs pf{};
     pf.l = l;
     pf.prefix = bt->prefill_prefix;
     pf.Hq = Hq;
@@ -523,19 +523,38 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     pf.base = 0;
     pf.err = e->err;
     pf.wait_ns = kWaitNs;
-    CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_pre_sms, s));
+  }
+  if (nd > 0) {
+    CF_CUDA(e, cudaEventRecord(e->ev_fork, s));
+    CF_CUDA(e, cudaStreamWaitEvent(e->dstream, e->ev_fork, 0));
+    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC0], e->dstream));
+    CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, da, n_dec_sms, e->dstream));
     e->launches++;
-    if (nd > 0) {
-      // Work-conserving split: once decode has finished, a second prefill
-      // grid on the decode stream takes the SMs it leaves and drains the same
-      // work queue.  Decode still owns its SMs for as long as it runs.
+    // every decode item has been taken when this grid ends (a second grid
+    // started later only takes items this one has not reached; it may still
+    // be finishing its last ones), so this is decode's time in the fork
+    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], e->dstream));
+    CF_CUDA(e, cudaEventRecord(e->ev_dec, e->dstream));
+    if (l > 0) {   // decode's SMs join prefill once decode is done
       CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_dec_sms, e->dstream));
       e->launches++;
     }
+    CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
+  }
+  if (l > 0) {
+    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE0], s));
+    CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_pre_sms, s));
+    e->launches++;
     if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE1], s));
+    if (nd > 0) {   // prefill's SMs join decode once prefill is done
+      CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, da, n_pre_sms, s));
+      e->launches++;
+    }
   }
   if (nd > 0) {
-    CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
+    CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_dec, 0));
+    CF_CUDA(e, launch_decode_merge(da, s));
+    e->launches++;
     CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_join, 0));
   }
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_JOIN], s));
@@ -668,6 +687,7 @@ cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride, co
   da.plan = e->plan;
   da.max_items = e->max_items;
   da.counter = e->dec_counter;
+  da.plan_ctas = e->sms;
   da.wait_ns = kWaitNs;
   da.err = e->err;
   CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, ctas, static_cast<cudaStream_t>(stream)));
@@ -880,6 +900,7 @@ cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* bt, const cf_kv_
   da.plan = e->plan;
   da.max_items = e->max_items;
   da.counter = e->dec_counter;
+  da.plan_ctas = e->sms;
   da.wait_ns = kWaitNs;
   da.err = e->err;
   cudaEvent_t t0, t1;

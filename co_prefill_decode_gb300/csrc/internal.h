@@ -124,14 +124,22 @@ struct DecodeArgs {
   int* plan;                      // [n + 2]: chunk prefix sums, chunk pages
   long long max_items;
   int* counter;                   // work-queue counter; 0 at launch, reset to 0 by the merge kernel
+  int plan_ctas;                  // CTA count the chunk plan is sized for (the device's SMs): the items,
+                                  // and so the results, depend on it, never on a launch's grid
   int* err;
   unsigned long long wait_ns;     // cap of one mbarrier wait
 };
 constexpr int kDecodeWarps = 8;
 long long decode_max_items(int max_decode, int Hkv, int max_ctas);
-// tmK/tmV: 2-D {d, pages*Hkv*ps} maps over the pools, box {64, 16}, 128-byte swizzle
+// tmK/tmV: 2-D {d, pages*Hkv*ps} maps over the pools, box {64, 16}, 128-byte swizzle.
+// launch_decode = launch_decode_kernel + launch_decode_merge.  Several
+// decode kernel grids may drain one work queue (same args); the merge must
+// follow all of them.
 cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a, int num_ctas,
                           cudaStream_t s);
+cudaError_t launch_decode_kernel(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a,
+                                 int num_ctas, cudaStream_t s);
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------------ prefill attention
 struct PrefillArgs {

@@ -129,7 +129,8 @@ void cf_destroy(cf_engine* e);
  *   Parallelism §4.3: rotary embeddings, append, attention);
  *   fork: decode attention (rows l..T-1) on a second stream with decode_sms
  *   SMs || causal prefill attention (rows 0..l-1) on `stream` with the rest;
- *   join; h = x + O W_o^T (fp32); hn = RMSNorm(h) g_ffn;
+ *   each path's SMs take over the other path's remaining work items once
+ *   their own path is done; join; h = x + O W_o^T (fp32); hn = RMSNorm(h) g_ffn;
  *   x_out = h + (silu(hn W_gate^T) * (hn W_up^T)) W_down^T.
  * x_in, x_out: bf16 [T][H], T = l + n_decode <= max_tokens; they must not
  * overlap.  The pool is modified (T new K/V rows).  The cached slots that
@@ -145,7 +146,9 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* b, const void* x_in, void*
  * q: bf16, row j at q + j * q_row_stride (elements), [Hq][d] inside the row.
  * n_keys: device int32 [n] (>= 1).  pages: device int32 [n][page_stride].
  * out: bf16, row j at out + j * out_row_stride, [Hq][d].
- * num_sms: CTAs of the persistent grid (0 = all SMs).
+ * num_sms: CTAs of the persistent grid (0 = all SMs).  The keys are cut
+ * into chunks planned for the device's full SM count, whatever num_sms is,
+ * so the output is bit-identical for every num_sms.
  * Uses the engine's workspace for the partials; n <= max_decode. */
 cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride,
                          const cf_kv_pool* pool, int n, const int* n_keys,

@@ -218,7 +218,8 @@ def test_decode_attention_matches_oracle(cf, name, shape, ctx, num_sms):
 
 def test_decode_split_count_and_page_order_invariance(cf):
     """Layout changes must not change results: a shuffled page table gives
-    bit-identical outputs; any split count agrees within fp32 rounding."""
+    bit-identical outputs, and so does any grid size (the chunk plan is
+    sized for the device, never for the launch)."""
     shape = wl.LLAMA8B
     ctx = (4000, 2500, 77)
     w = wl.Workload("inv", shape, len(ctx), ctx, 0, 0)
@@ -246,7 +247,7 @@ def test_decode_split_count_and_page_order_invariance(cf):
     torch.cuda.synchronize()
     assert torch.equal(outs[("a", 0)], outs[("b", 0)])
     assert torch.equal(outs[("a", 7)], outs[("b", 7)])
-    assert_close(outs[("a", 7)], f64(outs[("a", 0)]), "split count", 8e-3, 2e-4)
+    assert torch.equal(outs[("a", 7)], outs[("a", 0)])
 
 
 # --------------------------------------------------------------------- prefill

@@ -337,6 +337,6 @@ def test_layer_step_is_deterministic_and_launch_count(cf):
     S = LayerSetup(wl.reduced(wl.WORKLOADS["q14b"], (100, 9), 50, 10))
     n0 = S.eng.cf_launch_count()
     a = S.step().clone()
-    assert S.eng.cf_launch_count() - n0 == 10   # 9 stages + the second prefill grid of the fork
+    assert S.eng.cf_launch_count() - n0 == 11   # 9 stages + the fork's second decode and prefill grids
     b = S.step()
     assert torch.equal(a, b)
