@@ -87,6 +87,16 @@ CF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel in its stream is still running.  griddep_wait blocks
+// until that kernel has completed and its writes are visible; every kernel
+// here calls it before its first global write and before reading anything
+// an earlier kernel may have written (a no-op when launched normally).
+// griddep_launch lets the next such kernel start being scheduled.
+CF_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+CF_DEV void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 CF_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
   asm volatile(

@@ -278,6 +278,7 @@ cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const void* x, const CUten
   g.split_mode = e->split_mode;
   g.sk_ws = e->sk_ws;
   g.sk_flags = e->sk_flags;
+  g.b_static = 1;
   CF_CUDA(e, launch_gemm(tm_xn, e->tm.wqkv, e->tm.wqkv, g, e->sms, s));
   e->launches++;
   return CF_OK;
@@ -574,6 +575,7 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   g.split_mode = e->split_mode;
   g.sk_ws = e->sk_ws;
   g.sk_flags = e->sk_flags;
+  g.b_static = 1;
   CF_CUDA(e, launch_gemm(e->tm.attn, e->tm.wo, e->tm.wo, g, e->sms, s));
   e->launches++;
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_OPROJ], s));
@@ -596,6 +598,7 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   g.split_mode = e->split_mode;
   g.sk_ws = e->sk_ws;
   g.sk_flags = e->sk_flags;
+  g.b_static = 1;
   CF_CUDA(e, launch_gemm(e->tm.hn, e->tm.wg, e->tm.wu, g, e->sms, s));
   e->launches++;
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_GU], s));
@@ -615,6 +618,7 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   g.split_mode = e->split_mode;
   g.sk_ws = e->sk_ws;
   g.sk_flags = e->sk_flags;
+  g.b_static = 1;
   CF_CUDA(e, launch_gemm(e->tm.act, e->tm.wd, e->tm.wd, g, e->sms, s));
   e->launches++;
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_END], s));

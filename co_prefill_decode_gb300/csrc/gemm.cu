@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch();
   const uint32_t tmem_base = *tmem_holder;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
@@ -330,21 +331,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       UnitIter ui(blockIdx.x, gridDim.x, num_kb, p.tiles, p.dp_tiles, p.split);
       Unit u;
+      // Weight tiles of the first stages do not depend on the previous
+      // kernel: load them before waiting for it (the ring starts empty).
+      int pre = 0;
+      {
+        UnitIter first = ui;
+        Unit u0;
+        if (p.b_static && first.next(u0)) {
+          const int n0 = u0.tile / num_m;
+          const int brow0 = EPI == EPI_SWIGLU ? n0 * (BN / 2) : n0 * BN;
+          const int brow1 = EPI == EPI_SWIGLU ? brow0 : brow0 + BN / 2;
+          pre = u0.kb1 - u0.kb0 < STAGES ? u0.kb1 - u0.kb0 : STAGES;
+          for (int i = 0; i < pre; ++i) {
+            uint8_t* sb = smem + i * C::STAGE_BYTES + C::A_BYTES;
+            mbar_expect_tx(&full[i], C::STAGE_BYTES);
+            tma_load_2d(sb, &tmB0, &full[i], (u0.kb0 + i) * BK, brow0);
+            tma_load_2d(sb + C::B_BYTES / 2, &tmB1, &full[i], (u0.kb0 + i) * BK, brow1);
+          }
+        }
+      }
+      griddep_wait();
+      int n_issue = 0;
       while (ok && ui.next(u)) {
         const int mt = u.tile % num_m, nt = u.tile / num_m;
         const int brow0 = EPI == EPI_SWIGLU ? nt * (BN / 2) : nt * BN;
         const int brow1 = EPI == EPI_SWIGLU ? brow0 : brow0 + BN / 2;
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
-            ok = false;
-            break;
-          }
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++n_issue) {
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
-          mbar_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
-          tma_load_2d(sb, &tmB0, &full[stage], kb * BK, brow0);
-          tma_load_2d(sb + C::B_BYTES / 2, &tmB1, &full[stage], kb * BK, brow1);
+          if (n_issue < pre) {   // B already in flight: add A to the same stage
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
+            tma_load_2d(sb, &tmB0, &full[stage], kb * BK, brow0);
+            tma_load_2d(sb + C::B_BYTES / 2, &tmB1, &full[stage], kb * BK, brow1);
+          }
           last_phase[stage] = phase;
           issued_any = 1;
           if (++stage == STAGES) {
@@ -410,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r_in_tile = quarter * 32 + lane;
     const int ep_tid = threadIdx.x - 64;
+    griddep_wait();   // the epilogue reads the residual / RoPE table and writes
     int it = 0;
     UnitIter ui(blockIdx.x, gridDim.x, num_kb, p.tiles, p.dp_tiles, p.split);
     Unit u;
@@ -537,8 +564,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
   q.tiles = sc.tiles;
   q.dp_tiles = sc.dp_tiles;
   q.split = sc.split;
-  k<<<sc.grid, kThreads, C::SMEM, s>>>(a, b0, b1, q);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(sc.grid), dim3(kThreads), C::SMEM, s, a, b0, b1, q);
 }
 
 // Critical-path cost of the split-K fix-up, in k-blocks (one k-block of a

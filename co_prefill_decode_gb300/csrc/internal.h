@@ -9,6 +9,25 @@ namespace cf {
 
 constexpr int kPageSize = 16;
 
+// Launches `kernel` with programmatic stream serialisation: it may be
+// scheduled while the previous kernel of the stream finishes; the kernel
+// itself waits (griddep_wait) before touching data that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ------------------------------------------------------------------ GEMM
 enum GemmEpi {
   EPI_BF16 = 0,        // C bf16 = acc
@@ -46,6 +65,8 @@ struct GemmArgs {
   float* sk_ws;                   // [grid][BM * BN] fp32 partial tiles, one slot per CTA
   int* sk_flags;                  // [tail tiles]: partials stored; 0 between launches
   int tiles, dp_tiles, split;     // tiles [dp_tiles, tiles) are cut into `split` k-chunks
+  int b_static;                   // B is never written by other kernels: its first stages may be
+                                  // loaded before the previous kernel of the stream has finished
 };
 
 // Persistent schedule of one GEMM on `ctas` CTAs: whole BMxBN tiles for the

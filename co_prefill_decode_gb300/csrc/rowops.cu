@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
   const int row = blockIdx.x;
   const int H = a.H;
   __shared__ float red[kPrepThreads / 32];
+  griddep_wait();
+  griddep_launch();
   if (a.zero && row == 0 && threadIdx.x == 0) *a.zero = 0u;
   if (a.xn != nullptr) {
   float ss = 0.f;
@@ -145,9 +147,9 @@ __global__ void kv_append_kernel(const uint4* k, const uint4* v, int n, const in
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.in_f32)
-    prep_kernel<true><<<a.T, kPrepThreads, 0, s>>>(a);
+    return launch_pdl(prep_kernel<true>, dim3(a.T), dim3(kPrepThreads), 0, s, a);
   else
-    prep_kernel<false><<<a.T, kPrepThreads, 0, s>>>(a);
+    return launch_pdl(prep_kernel<false>, dim3(a.T), dim3(kPrepThreads), 0, s, a);
   return cudaGetLastError();
 }
 
