@@ -313,6 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_pref = dsm;                          // [n + 1]
   int* s_pages = dsm + kMaxDecodeReqs + 1;    // [n]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch();
+  if (!a.pdl) griddep_wait();
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(dsm) + kPlanBytes + kRingBytes);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDecodeWarps * R::STAGES; ++i) mbar_init(&bars[i], 1);
@@ -530,6 +532,7 @@ cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeA
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  if (a.pdl) return launch_pdl(decode_kernel<D, G16>, dim3(ctas), dim3(kThreads), kDecodeSmem, s, tk, tv, a);
   decode_kernel<D, G16><<<ctas, kThreads, kDecodeSmem, s>>>(tk, tv, a);
   return cudaGetLastError();
 }

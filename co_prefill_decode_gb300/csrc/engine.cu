@@ -537,7 +537,9 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], e->dstream));
     CF_CUDA(e, cudaEventRecord(e->ev_dec, e->dstream));
     if (l > 0) {   // decode's SMs join prefill once decode is done
-      CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_dec_sms, e->dstream));
+      PrefillArgs helper = pf;
+      helper.pdl = 1;   // starts on each SM decode frees
+      CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, helper, n_dec_sms, e->dstream));
       e->launches++;
     }
     CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
@@ -548,7 +550,9 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     e->launches++;
     if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE1], s));
     if (nd > 0) {   // prefill's SMs join decode once prefill is done
-      CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, da, n_pre_sms, s));
+      DecodeArgs helper = da;
+      helper.pdl = 1;   // starts on each SM prefill frees
+      CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, helper, n_pre_sms, s));
       e->launches++;
     }
   }

@@ -147,6 +147,9 @@ struct DecodeArgs {
   int* counter;                   // work-queue counter; 0 at launch, reset to 0 by the merge kernel
   int plan_ctas;                  // CTA count the chunk plan is sized for (the device's SMs): the items,
                                   // and so the results, depend on it, never on a launch's grid
+  int pdl;                        // launch with programmatic serialisation: the grid reads nothing the
+                                  // previous kernel of its stream writes, so it may start on SMs that
+                                  // kernel frees before it has finished
   int* err;
   unsigned long long wait_ns;     // cap of one mbarrier wait
 };
@@ -172,6 +175,7 @@ struct PrefillArgs {
   float scale_log2;
   unsigned* counter;              // work queue shared by the launches of one step
   unsigned base;                  // counter value at the start of this launch's queue (0)
+  int pdl;                        // as DecodeArgs::pdl
   int* err;
   unsigned long long wait_ns;
 };

@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(Split<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch();
+  if (!a.pdl) griddep_wait();
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -528,6 +530,7 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
     attr = true;
   }
   ctas = prefill_grid(a, ctas);
+  if (a.pdl) return launch_pdl(prefill_kernel<D>, dim3(ctas), dim3(Split<D>::THREADS), PfCfg<D>::SMEM, s, q, k, v, a);
   prefill_kernel<D><<<ctas, Split<D>::THREADS, PfCfg<D>::SMEM, s>>>(q, k, v, a);
   return cudaGetLastError();
 }
