@@ -805,6 +805,26 @@ cf_status cf_set_split_k(cf_engine* e, int split_mode) {
   return CF_OK;
 }
 
+cf_status cf_selftest_timeout(cf_engine* e, unsigned long long wait_ns, void* stream) {
+  if (!e || wait_ns == 0 || wait_ns > kWaitNs) return CF_ERR_INVALID_ARG;
+  const cf_config& c = e->cfg;
+  // one 128 x 256 tile: A = the engine's xn rows, B = the first W_qkv rows, C = its Q buffer
+  GemmArgs g{};
+  g.M = 128 < c.max_tokens ? 128 : c.max_tokens;
+  g.N = 256;
+  g.K = 64;
+  g.epi = EPI_BF16;
+  g.out = e->q;
+  g.ldo = 256;
+  g.err = e->err;
+  g.wait_ns = wait_ns;
+  g.split_mode = 1;
+  g.stall_test = 1;
+  CF_CUDA(e, launch_gemm(e->tm.xn, e->tm.wqkv, e->tm.wqkv, g, 1, static_cast<cudaStream_t>(stream)));
+  e->launches++;
+  return CF_OK;
+}
+
 cf_status cf_kv_append(cf_engine* e, const void* k, const void* v, int n, const int* slots, const cf_kv_pool* pool,
                        int n_kv_heads, int head_dim, int page_size, void* stream) {
   if (n < 0 || n_kv_heads <= 0 || page_size <= 0 || head_dim <= 0 || head_dim % 8)

@@ -158,6 +158,11 @@ CF_DEV int sk_fixup(uint32_t taddr, int r_in_tile, int ep_tid, const Unit& u, co
                     ws4 + (size_t)(j * tail + it) * kSlot4 + (size_t)(c0 + c) * (kPiece / 16), kPiece, fix_bar);
     }
     ok = mbar_wait(fix_bar, round & 1, wc);
+    if (!ok) {   // the bulk copies may still be landing in the ring: wait for them before leaving
+      volatile int dummy = 0;
+      const WaitCtl w2{&dummy, nullptr, p.wait_ns};
+      mbar_wait(fix_bar, round & 1, w2);
+    }
     if (ok) {
 #pragma unroll 1
       for (int c = 0; c < nc; ++c) {
@@ -379,13 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok && issued_any) {  // let our own copies land before the CTA exits
-        const WaitCtl drain_wc{abort_flag, nullptr, p.wait_ns};
+      // Let our own copies land before the CTA exits.  Normally the MMAs
+      // have consumed them and these phases are long complete; after an
+      // expired wait anywhere in the CTA they may still be in flight.
+      if (issued_any) {
         volatile int dummy = 0;
         const WaitCtl w2{&dummy, nullptr, p.wait_ns};
         for (int s = 0; s < STAGES; ++s)
           if (last_phase[s] != 0xffffffffu) mbar_wait(&full[s], last_phase[s], w2);
-        (void)drain_wc;
       }
     }
   } else if (warp == 1) {
@@ -396,6 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, issued = false;
       UnitIter ui(blockIdx.x, gridDim.x, num_kb, p.tiles, p.dp_tiles, p.split);
       Unit u;
+      // self-test: nothing arrives on `drain` before an MMA is issued, so this
+      // wait runs out, raises the abort flag and the timeout bit, and every
+      // role then winds down as after any expired wait
+      if (p.stall_test && !mbar_wait(drain, 0, wc)) ok = false;
       for (; ok && ui.next(u); ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;

@@ -67,6 +67,8 @@ struct GemmArgs {
   int tiles, dp_tiles, split;     // tiles [dp_tiles, tiles) are cut into `split` k-chunks
   int b_static;                   // B is never written by other kernels: its first stages may be
                                   // loaded before the previous kernel of the stream has finished
+  int stall_test;                 // failure-detection self-test: the MMA issuer first waits on a barrier
+                                  // nothing arrives at, so the bounded wait runs out
 };
 
 // Persistent schedule of one GEMM on `ctas` CTAs: whole BMxBN tiles for the

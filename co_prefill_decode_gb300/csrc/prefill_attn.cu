@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(Split<D>::THREADS, 1)
         pid = pid_next;
       }
     }
-    if (!ok && lane == 0) {  // let our own copies land before the CTA exits
+    // Let our own copies land before the CTA exits (normally consumed long
+    // ago; after an expired wait anywhere in the CTA they may be in flight).
+    if (lane == 0) {
       volatile int dummy = 0;
       const WaitCtl w2{&dummy, nullptr, a.wait_ns};
       if (last_q != 0xffffffffu) mbar_wait(q_full, last_q, w2);

@@ -109,6 +109,17 @@ typedef struct {
     const int* pre_pages;  /* device int32 [ceil((c_p + l) / page_size)]       */
 } cf_batch;
 
+/* Failure-detection self-test (no counterpart on the pages): launches one
+ * 128 x 256 GEMM tile on the engine's own buffers whose MMA-issuing thread
+ * first waits on an mbarrier that nothing arrives at.  The wait is bounded
+ * by wait_ns (1 ns .. 2 s); when it runs out the kernel sets the timeout bit
+ * of the device error word, lets its own TMA copies land, frees its tensor
+ * memory and returns, as any kernel here does after an expired wait.  The
+ * next cf_get_error reports CF_ERR_TIMEOUT and clears the word;
+ * the engine stays usable.  Overwrites workspace Q rows: do not run it
+ * during a layer step on another stream. */
+cf_status cf_selftest_timeout(cf_engine* e, unsigned long long wait_ns, void* stream);
+
 /* Largest number of SMs the device offers (0 if unknown).  No engine needed. */
 int cf_device_sm_count(void);
 

@@ -340,3 +340,23 @@ def test_layer_step_is_deterministic_and_launch_count(cf):
     assert S.eng.cf_launch_count() - n0 == 11   # 9 stages + the fork's second decode and prefill grids
     b = S.step()
     assert torch.equal(a, b)
+
+
+def test_bounded_wait_runs_out_and_the_engine_recovers(cf):
+    """Failure detection without a fault: cf_selftest_timeout makes a GEMM's
+    MMA thread wait on a barrier nothing arrives at; the 50 ms bound runs
+    out, the kernel raises the timeout bit, lets its copies land, frees its
+    tensor memory and returns.  The host reads the status, the word is
+    cleared, and the next layer step gives the same bits as before."""
+    S = LayerSetup(wl.reduced(wl.WORKLOADS["l8b"], (300, 64), 96, 40))
+    k0, v0 = S.kp.clone(), S.vp.clone()
+    ref = S.step().clone()
+    S.eng.cf_selftest_timeout(50_000_000)
+    st, msg = S.eng.cf_get_error()
+    assert st == cf.CF_ERR_TIMEOUT and "bounded wait expired" in msg
+    assert S.eng.cf_get_error()[0] == 0
+    S.kp.copy_(k0)
+    S.vp.copy_(v0)
+    assert torch.equal(S.step(), ref)
+    with pytest.raises(cf.CfError):
+        S.eng.cf_selftest_timeout(0)
