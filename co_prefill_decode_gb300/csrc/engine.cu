@@ -126,6 +126,7 @@ struct cf_engine {
   unsigned* counter;             // prefill work queue (set to 0 before each use)
   int* dec_counter;
   int split_mode = 0;            // GEMM split-K tail: 0 automatic, 1 off, >= 2 forced chunk count
+  int prefill_pair = 0;          // prefill items: 0 automatic, 1 single query tiles, 2 tile pairs
   float* sk_ws;                  // split-K partial tiles of the GEMMs
   int* sk_flags;                 // their per-tile flags (0 between launches)
   int* err;
@@ -520,7 +521,8 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     pf.out = e->attn;
     pf.out_stride = (long long)Hq * d;
     pf.scale_log2 = scale_log2;
-    pf.counter = e->counter;   // zeroed by this step's prep kernel
+    pf.pair = e->prefill_pair ? e->prefill_pair - 1 : prefill_pairing(pf.l, pf.Hq, e->sms);
+  pf.counter = e->counter;   // zeroed by this step's prep kernel
     pf.base = 0;
     pf.err = e->err;
     pf.wait_ns = kWaitNs;
@@ -732,6 +734,7 @@ cf_status cf_prefill_attn(cf_engine* e, const void* q, const cf_kv_pool* pool, i
   pf.out = static_cast<__nv_bfloat16*>(out);
   pf.out_stride = (long long)c.n_q_heads * c.head_dim;
   pf.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+  pf.pair = e->prefill_pair ? e->prefill_pair - 1 : prefill_pairing(pf.l, pf.Hq, e->sms);
   pf.counter = e->counter;
   pf.base = 0;
   CF_CUDA(e, cudaMemsetAsync(e->counter, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream)));
@@ -796,6 +799,12 @@ cf_status cf_gemm_schedule(int M, int N, int K, int epilogue, int ctas, int spli
   if (tiles) *tiles = sc.tiles;
   if (dp_tiles) *dp_tiles = sc.dp_tiles;
   if (split) *split = sc.split;
+  return CF_OK;
+}
+
+cf_status cf_set_prefill_pairing(cf_engine* e, int mode) {
+  if (!e || mode < 0 || mode > 2) return CF_ERR_INVALID_ARG;
+  e->prefill_pair = mode;
   return CF_OK;
 }
 

@@ -178,9 +178,17 @@ struct PrefillArgs {
   unsigned* counter;              // work queue shared by the launches of one step
   unsigned base;                  // counter value at the start of this launch's queue (0)
   int pdl;                        // as DecodeArgs::pdl
+  int pair;                       // items are pairs of query tiles sharing each K/V tile (1) or single
+                                  // tiles (0); every grid draining one queue must agree
   int* err;
   unsigned long long wait_ns;
 };
+// Pair query tiles when that still leaves at least one item per SM of the device.
+inline int prefill_pairing(int l, int Hq, int sms) {
+  const int n_qt = (l + 127) / 128;
+  return ((n_qt + 1) / 2) * Hq >= sms ? 1 : 0;
+}
+
 // CTAs a launch really uses (<= items), and the items of a launch.
 int prefill_grid(const PrefillArgs& a, int num_ctas);
 int prefill_items(const PrefillArgs& a);

@@ -109,6 +109,12 @@ typedef struct {
     const int* pre_pages;  /* device int32 [ceil((c_p + l) / page_size)]       */
 } cf_batch;
 
+/* Work items of prefill attention: 0 (default) pairs consecutive 128-row
+ * query tiles of a head, which share every K/V tile, when the chunk has at
+ * least one such pair per SM, else uses single tiles; 1 always single
+ * tiles; 2 always pairs.  Outputs are the same bits in every mode. */
+cf_status cf_set_prefill_pairing(cf_engine* e, int mode);
+
 /* Failure-detection self-test (no counterpart on the pages): launches one
  * 128 x 256 GEMM tile on the engine's own buffers whose MMA-issuing thread
  * first waits on an mbarrier that nothing arrives at.  The wait is bounded

@@ -262,7 +262,8 @@ PREFILL_CASES = [
 
 
 @pytest.mark.parametrize("name,shape,l,cp", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
-def test_prefill_attention_matches_oracle(cf, name, shape, l, cp):
+@pytest.mark.parametrize("pairing", [0, 2])
+def test_prefill_attention_matches_oracle(cf, name, shape, l, cp, pairing):
     w = wl.Workload(name, shape, 0, (), l, cp)
     b = wl.make_batch(w, 4)
     kp, vp = wl.make_pools(w, b, 4, "cuda")
@@ -271,11 +272,36 @@ def test_prefill_attention_matches_oracle(cf, name, shape, l, cp):
     q = randn_bf16((l, Hq, d), 14)
     out = torch.zeros((l, Hq, d), dtype=torch.bfloat16, device="cuda")
     eng = engine_for(cf, shape)
+    eng.cf_set_prefill_pairing(pairing)   # automatic (single tiles at these sizes), or tile pairs
     ref = oracle.prefill_attention(f64(q), kp, vp, cp, b.pre_pages, 16)
     eng.cf_prefill_attn(q, cf.pool_of(kp, vp), l, cp, torch.as_tensor(b.pre_pages, device="cuda"), out)
     torch.cuda.synchronize()
     assert eng.cf_get_error()[0] == 0
     assert_close(out, ref, f"prefill {name}")
+
+
+@pytest.mark.parametrize("name,shape,l,cp", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_prefill_pairs_change_no_bit(cf, name, shape, l, cp):
+    """Items that pair two query tiles sharing each K/V tile compute every
+    tile exactly as single-tile items do (same key order, same MMAs)."""
+    w = wl.Workload(name, shape, 0, (), l, cp)
+    b = wl.make_batch(w, 4)
+    kp, vp = wl.make_pools(w, b, 4, "cuda")
+    Hq, d = shape.n_q_heads, shape.head_dim
+    q = randn_bf16((l, Hq, d), 41)
+    fill_positions(kp, vp, b.pre_pages, cp, l, 42)
+    eng = engine_for(cf, shape)
+    pages = torch.as_tensor(b.pre_pages, device="cuda")
+    outs = []
+    for mode in (1, 2):
+        eng.cf_set_prefill_pairing(mode)
+        o = torch.full((l, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        eng.cf_prefill_attn(q, cf.pool_of(kp, vp), l, cp, pages, o)
+        outs.append(o)
+    eng.cf_set_prefill_pairing(0)
+    torch.cuda.synchronize()
+    assert eng.cf_get_error()[0] == 0
+    assert torch.equal(outs[0], outs[1])
 
 
 def test_prefill_equals_decode_for_last_row(cf):
