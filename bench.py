@@ -36,7 +36,7 @@ METRIC = "co-batched layer step µs & tokens/s; decode attn % HBM peak; GEMM % B
 # DRAM bytes (read + write) per launch of the roofline kernel, from one ncu
 # capture of the same kernel build; cleared whenever that kernel changes.
 DOMINANT_TRAFFIC = {
-    "l8b": {"bytes": 243670272 + 21712640, "source": "profiles/gemm_gateup_l8b_T1040.md"},
+    "l8b": {"bytes": 243602944 + 22031872, "source": "profiles/gemm_gateup_l8b_T1040.md"},
 }
 
 
@@ -416,7 +416,8 @@ def run_kernel_case(args):
 
     decode : decode attention, Qwen3-32B shape, 8 requests x 8192 cached keys
              (268 MB of KV, larger than L2)
-    prefill: prefill attention, Qwen3-32B shape, 512-token chunk on 4096 cached
+    prefill: prefill attention, Qwen3-32B shape, 2048-token chunk on 4096 cached
+             (8 query-tile pairs x 64 heads: several waves of paired items)
     gemm   : gate/up GEMM + SwiGLU epilogue of the Llama-3.1-8B layer, T = 1040
     """
     import numpy as np
@@ -429,13 +430,13 @@ def run_kernel_case(args):
     if which == "decode":
         w = wl.Workload("k", s, 8, (8192,) * 8, 0, 0)
     elif which == "prefill":
-        w = wl.Workload("k", s, 0, (), 512, 4096)
+        w = wl.Workload("k", s, 0, (), 2048, 4096)
     else:
         w = wl.Workload("k", s, 0, (), 1040, 0)
     b = wl.make_batch(w, args.seed)
     kp, vp = wl.make_pools(w, b, args.seed, "cuda")
     W = wl.make_weights(wl.Workload("k", s, 1, (1,), 0, 0), args.seed, "cuda", unit_gains=True)
-    eng = cf.Engine(cf.make_config(s, 2048, 64), W)
+    eng = cf.Engine(cf.make_config(s, 4096, 64), W)
     pool = cf.pool_of(kp, vp)
     Hq, d = s.n_q_heads, s.head_dim
     g = torch.Generator(device="cuda").manual_seed(args.seed)
