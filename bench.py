@@ -232,6 +232,7 @@ def run_cf(args, rank, world, local, pg):
     kp, vp = wl.make_pools(w, b, args.seed, "cuda")
     T = b.n_tokens
     eng = cf.Engine(cf.make_config(w.shape, T, max(b.n_decode, 1), args.decode_sms), W)
+    eng.cf_set_graphs(args.graphs)   # piecewise CUDA graphs of the linear segments
     dec_ctx = torch.as_tensor(b.dec_ctx, device=dev)
     dec_pages = torch.as_tensor(b.dec_pages, device=dev)
     pre_pages = torch.as_tensor(b.pre_pages if len(b.pre_pages) else np.zeros(1, np.int32), device=dev)
@@ -358,7 +359,7 @@ def run_cf(args, rank, world, local, pg):
         "warmup": args.warmup, "ms_per_step": ms_step, "layer_step_us": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations and KV)",
-        "config": workload_config(w, b, world),
+        "config": dict(workload_config(w, b, world), graphs=bool(args.graphs)),
         "decode_attn_hbm_frac": (kern["decode_attn"]["gbs"] or 0) / peaks["hbm_gbs"],
         "gemm_bf16_frac": gemm_tflops / peak_tc,
         "prefill_attn_bf16_frac": (kern["prefill_attn"]["tflops"] or 0) / peak_tc,
@@ -512,6 +513,8 @@ def main(argv=None):
     ap.add_argument("--decode-sms", type=int, default=0)
     ap.add_argument("--sweep-decode-sms", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graphs", type=int, default=0, choices=[0, 1],
+                    help="replay the linear segments of the step as CUDA graphs (1) or launch eagerly (0)")
     ap.add_argument("--kernel", choices=["decode", "prefill", "gemm"], default=None,
                     help="run one small launch of one kernel (for ncu) instead of the benchmark")
     args = ap.parse_args(argv)

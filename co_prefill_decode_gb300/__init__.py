@@ -28,7 +28,7 @@ EXPORTS = (
     "cf_prefill_attn", "cf_gemm", "cf_kv_append", "cf_get_error", "cf_engine_buffer",
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
-    "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_selftest_timeout", "cf_set_prefill_pairing",
+    "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
 )
 
 
@@ -99,6 +99,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_set_split_k": (I, [P, I]),
         "cf_selftest_timeout": (I, [P, ctypes.c_ulonglong, P]),
         "cf_set_prefill_pairing": (I, [P, I]),
+        "cf_set_graphs": (I, [P, I]),
+        "cf_graph_captures": (L, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -243,6 +245,12 @@ class Engine:
 
     def cf_set_decode_sms(self, n: int):
         _check(self.lib, self.handle, self.lib.cf_set_decode_sms(self.handle, n))
+
+    def cf_set_graphs(self, on: bool):
+        _check(self.lib, self.handle, self.lib.cf_set_graphs(self.handle, int(on)))
+
+    def cf_graph_captures(self) -> int:
+        return int(self.lib.cf_graph_captures(self.handle))
 
     def cf_set_prefill_pairing(self, mode: int):
         """0: automatic, 1: single query tiles, 2: tile pairs sharing each K/V tile."""

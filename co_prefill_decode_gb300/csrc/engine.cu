@@ -144,6 +144,20 @@ struct cf_engine {
   double phase_ms[kPhases] = {0};
   int phase_steps = 0;
   std::vector<std::pair<int, float>> calib;   // (decode CTAs, ms) of the last calibration
+  // piecewise CUDA graphs of the shared linear segments (ConfluxServe §6.1, Fig. 10)
+  int use_graphs = 0;
+  cudaStream_t cstream = nullptr;    // capture stream
+  int* bdev = nullptr;               // device batch descriptor: chunk length, prefix
+  struct Graphs {
+    long long T;
+    const void *x_in, *x_out, *pk, *pv;
+    int num_pages;
+    const int *dec_ctx, *dec_pages, *pre_pages;
+    int dec_stride, split_mode;
+    cudaGraphExec_t a, b;            // RMSNorm + QKV; O-proj + RMSNorm + gate/up + down
+  };
+  std::vector<Graphs> graphs;
+  long long graph_captures = 0;
 };
 
 namespace {
@@ -226,7 +240,7 @@ cf_status check_batch(cf_engine* e, const cf_batch* bt) {
 // RoPE table + slots (and optionally the RMSNorm of x), then the fused QKV
 // GEMM whose epilogue writes q and appends k, v.
 cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const void* x, const CUtensorMap& tm_xn, void* q_out,
-                    const cf_kv_pool* pool, cudaStream_t s, cudaEvent_t ev_mid) {
+                    const cf_kv_pool* pool, cudaStream_t s, cudaEvent_t ev_mid, const int* bdev = nullptr) {
   const cf_config& c = e->cfg;
   const int T = bt->prefill_len + bt->n_decode;
   PrepArgs pa{};
@@ -252,6 +266,7 @@ cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const void* x, const CUten
   pa.page_size = c.page_size;
   pa.err = e->err;
   pa.zero = e->counter;   // the prefill work queue of this step starts at 0
+  pa.bdev = bdev;
   CF_CUDA(e, launch_prep(pa, s));
   e->launches++;
   if (ev_mid) CF_CUDA(e, cudaEventRecord(ev_mid, s));
@@ -365,7 +380,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   const size_t o_cs = take(T * (d / 2) * 8), o_slot = take(T * 4), o_inv = take(d / 2 * 8);
   const size_t o_po = take((size_t)e->max_items * G * d * 4), o_pml = take((size_t)e->max_items * G * 2 * 4);
   const size_t o_plan = take((size_t)(c.max_decode + 4) * 4), o_cnt = take(4), o_err = take(4);
-  const size_t o_dcnt = take(4);
+  const size_t o_dcnt = take(4), o_bdev = take(16);
   const size_t o_skw = take(gemm_sk_ws_bytes(e->sms)), o_skf = take(gemm_sk_flag_bytes(e->sms));
   e->ws_bytes = off;
   if (cudaMalloc(&e->ws, off) != cudaSuccess) {
@@ -389,6 +404,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   e->counter = reinterpret_cast<unsigned*>(b + o_cnt);
   e->err = reinterpret_cast<int*>(b + o_err);
   e->dec_counter = reinterpret_cast<int*>(b + o_dcnt);
+  e->bdev = reinterpret_cast<int*>(b + o_bdev);
   e->sk_ws = reinterpret_cast<float*>(b + o_skw);
   e->sk_flags = reinterpret_cast<int*>(b + o_skf);
   bool ok = cudaMemset(e->ws, 0, off) == cudaSuccess;
@@ -397,6 +413,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   for (size_t i = 0; i < d / 2; ++i) inv[i] = pow((double)c.rope_theta, -2.0 * (double)i / (double)d);
   ok = ok && cudaMemcpy(e->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaStreamCreateWithFlags(&e->dstream, cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaStreamCreateWithFlags(&e->cstream, cudaStreamNonBlocking) == cudaSuccess;
   ok = ok && cudaEventCreateWithFlags(&e->ev_fork, cudaEventDisableTiming) == cudaSuccess;
   ok = ok && cudaEventCreateWithFlags(&e->ev_join, cudaEventDisableTiming) == cudaSuccess;
   ok = ok && cudaEventCreateWithFlags(&e->ev_dec, cudaEventDisableTiming) == cudaSuccess;
@@ -429,8 +446,131 @@ void cf_destroy(cf_engine* e) {
   if (e->ev_join) cudaEventDestroy(e->ev_join);
   if (e->ev_dec) cudaEventDestroy(e->ev_dec);
   if (e->dstream) cudaStreamDestroy(e->dstream);
+  for (auto& g : e->graphs) {
+    if (g.a) cudaGraphExecDestroy(g.a);
+    if (g.b) cudaGraphExecDestroy(g.b);
+  }
+  if (e->cstream) cudaStreamDestroy(e->cstream);
   if (e->ws) cudaFree(e->ws);
   delete e;
+}
+
+// a6 - a9: O-proj + residual -> h (fp32), RMSNorm, gate/up + SwiGLU, down +
+// residual -> x_out.  Depends on the batch only through T.
+cf_status ffn_stage(cf_engine* e, long long T, const void* x_in, void* x_out, cudaStream_t s, cudaEvent_t* ev) {
+  const cf_config& c = e->cfg;
+  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, F = c.ffn_dim;
+  cf_status st = CF_OK;
+  // a6: O-proj + residual -> h (fp32)
+  GemmArgs g{};
+  g.M = (int)T;
+  g.N = H;
+  g.K = Hq * d;
+  g.epi = EPI_RESID_F32;
+  g.out = e->h;
+  g.ldo = H;
+  g.aux = x_in;
+  g.ld_aux = H;
+  g.err = e->err;
+  g.wait_ns = kWaitNs;
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
+  g.b_static = 1;
+  CF_CUDA(e, launch_gemm(e->tm.attn, e->tm.wo, e->tm.wo, g, e->sms, s));
+  e->launches++;
+  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_OPROJ], s));
+
+  // a7: RMSNorm of h
+  st = rmsnorm_stage(e, e->h, 1, e->w.g_ffn, e->hn, (int)T, s);
+  if (st != CF_OK) return st;
+  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PREP2], s));
+
+  // a8: gate/up GEMM + SwiGLU
+  g = GemmArgs{};
+  g.M = (int)T;
+  g.N = F;
+  g.K = H;
+  g.epi = EPI_SWIGLU;
+  g.out = e->act;
+  g.ldo = F;
+  g.err = e->err;
+  g.wait_ns = kWaitNs;
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
+  g.b_static = 1;
+  CF_CUDA(e, launch_gemm(e->tm.hn, e->tm.wg, e->tm.wu, g, e->sms, s));
+  e->launches++;
+  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_GU], s));
+
+  // a9: down GEMM + residual -> x_out
+  g = GemmArgs{};
+  g.M = (int)T;
+  g.N = H;
+  g.K = F;
+  g.epi = EPI_RESID_BF16;
+  g.out = x_out;
+  g.ldo = H;
+  g.aux = e->h;
+  g.ld_aux = H;
+  g.err = e->err;
+  g.wait_ns = kWaitNs;
+  g.split_mode = e->split_mode;
+  g.sk_ws = e->sk_ws;
+  g.sk_flags = e->sk_flags;
+  g.b_static = 1;
+  CF_CUDA(e, launch_gemm(e->tm.act, e->tm.wd, e->tm.wd, g, e->sms, s));
+  e->launches++;
+  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_END], s));
+  return CF_OK;
+}
+
+// The graphs of one (T, buffers) key, captured on first use.
+cf_engine::Graphs* graphs_for(cf_engine* e, const cf_batch* bt, long long T, const void* x_in, void* x_out,
+                              const cf_kv_pool* pool, cf_status* st) {
+  *st = CF_OK;
+  for (auto& g : e->graphs)
+    if (g.T == T && g.x_in == x_in && g.x_out == x_out && g.pk == pool->k && g.pv == pool->v &&
+        g.num_pages == pool->num_pages && g.dec_ctx == bt->dec_ctx && g.dec_pages == bt->dec_pages &&
+        g.pre_pages == bt->pre_pages && g.dec_stride == bt->dec_stride && g.split_mode == e->split_mode)
+      return &g;
+  if (e->graphs.size() >= 16) {   // keep the cache small: drop the oldest
+    cudaGraphExecDestroy(e->graphs.front().a);
+    cudaGraphExecDestroy(e->graphs.front().b);
+    e->graphs.erase(e->graphs.begin());
+  }
+  cf_engine::Graphs g{T, x_in, x_out, pool->k, pool->v, pool->num_pages, bt->dec_ctx, bt->dec_pages,
+                      bt->pre_pages, bt->dec_stride, e->split_mode, nullptr, nullptr};
+  const long long launches = e->launches;   // captured launches do not run now
+  cudaGraph_t ga = nullptr, gb = nullptr;
+  cudaError_t r = cudaStreamBeginCapture(e->cstream, cudaStreamCaptureModeThreadLocal);
+  if (r == cudaSuccess) {
+    *st = qkv_stage(e, bt, x_in, e->tm.xn, e->q, pool, e->cstream, nullptr, e->bdev);
+    r = cudaStreamEndCapture(e->cstream, &ga);
+  }
+  if (r == cudaSuccess && *st == CF_OK) {
+    r = cudaStreamBeginCapture(e->cstream, cudaStreamCaptureModeThreadLocal);
+    if (r == cudaSuccess) {
+      *st = ffn_stage(e, T, x_in, x_out, e->cstream, nullptr);
+      r = cudaStreamEndCapture(e->cstream, &gb);
+    }
+  }
+  if (r == cudaSuccess && *st == CF_OK) r = cudaGraphInstantiate(&g.a, ga, 0);
+  if (r == cudaSuccess && *st == CF_OK) r = cudaGraphInstantiate(&g.b, gb, 0);
+  if (ga) cudaGraphDestroy(ga);
+  if (gb) cudaGraphDestroy(gb);
+  e->launches = launches;
+  if (r != cudaSuccess || *st != CF_OK) {
+    if (g.a) cudaGraphExecDestroy(g.a);
+    if (g.b) cudaGraphExecDestroy(g.b);
+    cudaGetLastError();
+    if (*st == CF_OK) *st = cuda_fail(e, r, "graph capture");
+    return nullptr;
+  }
+  e->graph_captures++;
+  e->graphs.push_back(g);
+  return &e->graphs.back();
 }
 
 cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void* x_out, const cf_kv_pool* pool,
@@ -451,7 +591,7 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   st = pool_maps(e, pool);
   if (st != CF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, F = c.ffn_dim;
+  const int d = c.head_dim, Hq = c.n_q_heads;
 
   cudaEvent_t* ev = nullptr;
   int slot = -1;
@@ -466,9 +606,24 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     CF_CUDA(e, cudaEventRecord(ev[EV_START], s));
   }
 
-  // a1 + a2: RMSNorm (+ RoPE table, slots), fused QKV GEMM with append
-  st = qkv_stage(e, bt, x_in, e->tm.xn, e->q, pool, s, ev ? ev[EV_PREP] : nullptr);
-  if (st != CF_OK) return st;
+  // a1 + a2: RMSNorm (+ RoPE table, slots), fused QKV GEMM with append.
+  // With graphs on, this segment and a6 - a9 replay captured graphs; the
+  // batch's chunk length and prefix reach the captured RMSNorm kernel through
+  // a small device descriptor written just before.
+  cf_engine::Graphs* ge = nullptr;
+  if (e->use_graphs && !ev) {
+    ge = graphs_for(e, bt, T, x_in, x_out, pool, &st);
+    if (st != CF_OK) return st;
+  }
+  if (ge) {
+    const int hb[2] = {l, bt->prefill_prefix};
+    CF_CUDA(e, cudaMemcpyAsync(e->bdev, hb, sizeof(hb), cudaMemcpyHostToDevice, s));
+    CF_CUDA(e, cudaGraphLaunch(ge->a, s));
+    e->launches += 2;
+  } else {
+    st = qkv_stage(e, bt, x_in, e->tm.xn, e->q, pool, s, ev ? ev[EV_PREP] : nullptr);
+    if (st != CF_OK) return st;
+  }
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_QKV], s));
 
   // a3 || a4: the attention fork.  Decode runs on a second stream with
@@ -566,69 +721,13 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   }
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_JOIN], s));
 
-  // a6: O-proj + residual -> h (fp32)
-  GemmArgs g{};
-  g.M = (int)T;
-  g.N = H;
-  g.K = Hq * d;
-  g.epi = EPI_RESID_F32;
-  g.out = e->h;
-  g.ldo = H;
-  g.aux = x_in;
-  g.ld_aux = H;
-  g.err = e->err;
-  g.wait_ns = kWaitNs;
-  g.split_mode = e->split_mode;
-  g.sk_ws = e->sk_ws;
-  g.sk_flags = e->sk_flags;
-  g.b_static = 1;
-  CF_CUDA(e, launch_gemm(e->tm.attn, e->tm.wo, e->tm.wo, g, e->sms, s));
-  e->launches++;
-  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_OPROJ], s));
-
-  // a7: RMSNorm of h
-  st = rmsnorm_stage(e, e->h, 1, e->w.g_ffn, e->hn, (int)T, s);
-  if (st != CF_OK) return st;
-  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PREP2], s));
-
-  // a8: gate/up GEMM + SwiGLU
-  g = GemmArgs{};
-  g.M = (int)T;
-  g.N = F;
-  g.K = H;
-  g.epi = EPI_SWIGLU;
-  g.out = e->act;
-  g.ldo = F;
-  g.err = e->err;
-  g.wait_ns = kWaitNs;
-  g.split_mode = e->split_mode;
-  g.sk_ws = e->sk_ws;
-  g.sk_flags = e->sk_flags;
-  g.b_static = 1;
-  CF_CUDA(e, launch_gemm(e->tm.hn, e->tm.wg, e->tm.wu, g, e->sms, s));
-  e->launches++;
-  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_GU], s));
-
-  // a9: down GEMM + residual -> x_out
-  g = GemmArgs{};
-  g.M = (int)T;
-  g.N = H;
-  g.K = F;
-  g.epi = EPI_RESID_BF16;
-  g.out = x_out;
-  g.ldo = H;
-  g.aux = e->h;
-  g.ld_aux = H;
-  g.err = e->err;
-  g.wait_ns = kWaitNs;
-  g.split_mode = e->split_mode;
-  g.sk_ws = e->sk_ws;
-  g.sk_flags = e->sk_flags;
-  g.b_static = 1;
-  CF_CUDA(e, launch_gemm(e->tm.act, e->tm.wd, e->tm.wd, g, e->sms, s));
-  e->launches++;
-  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_END], s));
-  return CF_OK;
+  // a6 - a9
+  if (ge) {
+    CF_CUDA(e, cudaGraphLaunch(ge->b, s));
+    e->launches += 4;
+    return CF_OK;
+  }
+  return ffn_stage(e, T, x_in, x_out, s, ev);
 }
 
 cf_status cf_rmsnorm(cf_engine* e, const void* x, int x_is_f32, const void* gain, void* out, int T, void* stream) {
@@ -807,6 +906,14 @@ cf_status cf_set_prefill_pairing(cf_engine* e, int mode) {
   e->prefill_pair = mode;
   return CF_OK;
 }
+
+cf_status cf_set_graphs(cf_engine* e, int enable) {
+  if (!e) return CF_ERR_INVALID_ARG;
+  e->use_graphs = enable ? 1 : 0;
+  return CF_OK;
+}
+
+long long cf_graph_captures(cf_engine* e) { return e ? e->graph_captures : 0; }
 
 cf_status cf_set_split_k(cf_engine* e, int split_mode) {
   if (!e || split_mode < 0) return CF_ERR_INVALID_ARG;

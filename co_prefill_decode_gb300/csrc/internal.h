@@ -119,6 +119,7 @@ struct PrepArgs {
   int num_pages, page_size;
   int* err;
   unsigned* zero;                 // if set, block 0 stores 0 here (resets a work queue)
+  const int* bdev;                // if set, l and prefix are read from bdev[0], bdev[1] (graph replay)
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 

@@ -81,16 +81,19 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
   }
   if (a.rope_cs == nullptr) return;
 
-  // position and pool slot of this row
+  // position and pool slot of this row; a replayed graph reads the chunk
+  // length and prefix of the current batch from device memory
+  const int l = a.bdev ? a.bdev[0] : a.l;
+  const int prefix = a.bdev ? a.bdev[1] : a.prefix;
   long long pos;
   const int* table;
   int table_len;
-  if (row < a.l) {
-    pos = (long long)a.prefix + row;
+  if (row < l) {
+    pos = (long long)prefix + row;
     table = a.pre_pages;
-    table_len = (a.prefix + a.l + a.page_size - 1) / a.page_size;
+    table_len = (prefix + l + a.page_size - 1) / a.page_size;
   } else {
-    const int j = row - a.l;
+    const int j = row - l;
     pos = a.dec_ctx[j];
     table = a.dec_pages + (size_t)j * a.dec_stride;
     table_len = a.dec_stride;

@@ -109,6 +109,20 @@ typedef struct {
     const int* pre_pages;  /* device int32 [ceil((c_p + l) / page_size)]       */
 } cf_batch;
 
+/* Piecewise CUDA graphs (ConfluxServe §6.1, Fig. 10), off by default.  When
+ * on, cf_layer_step captures its two shared linear segments (RMSNorm + fused
+ * QKV; O-proj + RMSNorm + gate/up + down) as CUDA graphs on first use and
+ * replays them, while the attention fork between them is launched eagerly.
+ * The graphs depend on T and on the buffers (x_in, x_out, pool, page tables):
+ * a batch with the same T and buffers but another split into chunk and
+ * decode rows, other prefix or other context lengths reuses them (the chunk
+ * length and prefix reach the captured kernels through device memory).  Up
+ * to 16 keys are cached; steps with profiling on run eagerly.  Outputs are
+ * the same bits as eager steps. */
+cf_status cf_set_graphs(cf_engine* e, int enable);
+/* Number of graph pairs this engine has captured so far. */
+long long cf_graph_captures(cf_engine* e);
+
 /* Work items of prefill attention: 0 (default) pairs consecutive 128-row
  * query tiles of a head, which share every K/V tile, when the chunk has at
  * least one such pair per SM, else uses single tiles; 1 always single

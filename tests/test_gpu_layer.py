@@ -360,3 +360,41 @@ def test_bounded_wait_runs_out_and_the_engine_recovers(cf):
     assert torch.equal(S.step(), ref)
     with pytest.raises(cf.CfError):
         S.eng.cf_selftest_timeout(0)
+
+
+def test_layer_step_graphs_match_eager(cf):
+    """Piecewise CUDA graphs (ConfluxServe §6.1, Fig. 10): the replayed
+    segments give the eager step's bits; a batch with the same rows and
+    buffers but another prefix and other decode contexts replays the same
+    graphs (the chunk length and prefix reach them through device memory)."""
+    S = LayerSetup(wl.reduced(wl.WORKLOADS["l8b"], (300, 64, 1000), 96, 40))
+    k0, v0 = S.kp.clone(), S.vp.clone()
+
+    out = torch.empty_like(S.x)   # one output buffer: the graphs are keyed by the buffers
+
+    def run(batch, graphs):
+        S.kp.copy_(k0)
+        S.vp.copy_(v0)
+        S.eng.cf_set_graphs(graphs)
+        out.fill_(float("nan"))
+        S.eng.cf_layer_step(batch, S.x, out, S.pool)
+        torch.cuda.synchronize()
+        assert S.eng.cf_get_error()[0] == 0
+        return out.clone()
+
+    eager = run(S.batch, False)
+    n0 = S.eng.cf_graph_captures()
+    g1 = run(S.batch, True)
+    g2 = run(S.batch, True)
+    assert S.eng.cf_graph_captures() == n0 + 1
+    assert torch.equal(g1, eager) and torch.equal(g2, eager)
+    # same rows and buffers, another prefix and shorter decode contexts
+    ctx2 = (S.dec_ctx // 2).contiguous()
+    S.dec_ctx.copy_(ctx2)
+    b2 = cf.batch_of(S.b.n_decode, S.dec_ctx, S.dec_pages, S.b.prefill_len, 24, S.pre_pages)
+    eager2 = run(b2, False)
+    graph2 = run(b2, True)
+    assert S.eng.cf_graph_captures() == n0 + 1
+    assert torch.equal(graph2, eager2)
+    assert not torch.equal(eager2, eager)
+    S.eng.cf_set_graphs(False)
