@@ -29,6 +29,7 @@ EXPORTS = (
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
     "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
+    "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate",
 )
 
 
@@ -58,6 +59,19 @@ class cf_batch(ctypes.Structure):
     _fields_ = [("n_decode", ctypes.c_int), ("dec_ctx", ctypes.c_void_p), ("dec_pages", ctypes.c_void_p),
                 ("dec_stride", ctypes.c_int), ("prefill_len", ctypes.c_int), ("prefill_prefix", ctypes.c_int),
                 ("pre_pages", ctypes.c_void_p)]
+
+
+class cf_latency_model(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in
+                ("gamma", "gamma0", "a_d", "a_d0", "a_p", "a_p0", "a_comm", "a_comm0", "alpha", "beta")]
+
+
+class cf_rank_load(ctypes.Structure):
+    _fields_ = [("n_prefill", ctypes.c_longlong), ("n_decode", ctypes.c_longlong), ("ctx_sum", ctypes.c_double)]
+
+
+class cf_latency_parts(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in ("t_iter", "t_gemm", "t_attn", "t_prefill", "t_decode")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -101,6 +115,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_set_prefill_pairing": (I, [P, I]),
         "cf_set_graphs": (I, [P, I]),
         "cf_graph_captures": (L, [P]),
+        "cf_latency_predict": (I, [ctypes.POINTER(cf_latency_model), I, ctypes.POINTER(cf_rank_load), I,
+                                   ctypes.POINTER(L), ctypes.POINTER(L), I, ctypes.POINTER(cf_latency_parts)]),
+        "cf_latency_fit_line": (I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), I,
+                                    ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
+        "cf_latency_calibrate": (I, [ctypes.POINTER(cf_latency_model), I] + [ctypes.POINTER(ctypes.c_double)] * 4
+                                 + [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -318,3 +338,50 @@ def batch_of(n_decode: int, dec_ctx, dec_pages, prefill_len: int, prefill_prefix
     stride = int(dec_pages.shape[1]) if dec_pages is not None and dec_pages.dim() == 2 else 1
     return cf_batch(n_decode, _ptr(dec_ctx) if n_decode else None, _ptr(dec_pages) if n_decode else None, stride,
                     prefill_len, prefill_prefix, _ptr(pre_pages) if prefill_len else None)
+
+
+# ---------------------------------------------------------------------------
+# Iteration-latency estimator (host code in libcf; no GPU needed)
+# ---------------------------------------------------------------------------
+def _doubles(v):
+    v = [float(x) for x in v]
+    return (ctypes.c_double * max(len(v), 1))(*v), len(v)
+
+
+def cf_latency_predict(model: cf_latency_model, ranks, chunks=(), n_layers: int = 1) -> Dict[str, float]:
+    """ranks: [(n_prefill, n_decode, ctx_sum)] per rank; chunks: [(l_i, c_i)].
+    Returns t_iter, t_gemm, t_attn, t_prefill, t_decode."""
+    lib = load_library()
+    rk = (cf_rank_load * max(len(ranks), 1))(*[cf_rank_load(int(a), int(b), float(c)) for a, b, c in ranks])
+    cl = (ctypes.c_longlong * max(len(chunks), 1))(*[int(l) for l, _ in chunks])
+    cc = (ctypes.c_longlong * max(len(chunks), 1))(*[int(c) for _, c in chunks])
+    out = cf_latency_parts()
+    _check(lib, None, lib.cf_latency_predict(ctypes.byref(model), len(ranks), rk, len(chunks), cl, cc,
+                                             int(n_layers), ctypes.byref(out)))
+    return {n: getattr(out, n) for n, _ in cf_latency_parts._fields_}
+
+
+def cf_latency_fit_line(x, y):
+    """Least-squares (slope, intercept) of y on x."""
+    lib = load_library()
+    xa, n = _doubles(x)
+    ya, m = _doubles(y)
+    if n != m:
+        raise ValueError("x and y differ in length")
+    slope, icpt = ctypes.c_double(), ctypes.c_double()
+    _check(lib, None, lib.cf_latency_fit_line(xa, ya, n, ctypes.byref(slope), ctypes.byref(icpt)))
+    return slope.value, icpt.value
+
+
+def cf_latency_calibrate(model: cf_latency_model, t_gemm, t_prefill, t_decode, t_meas,
+                         f_max: float = 3.0, step: float = 0.01) -> float:
+    """Sets model.alpha / model.beta from co-batched profiles; returns the MAPE (%)."""
+    lib = load_library()
+    arrs = [_doubles(v) for v in (t_gemm, t_prefill, t_decode, t_meas)]
+    n = arrs[0][1]
+    if any(a[1] != n for a in arrs):
+        raise ValueError("profiles differ in length")
+    err = ctypes.c_double()
+    _check(lib, None, lib.cf_latency_calibrate(ctypes.byref(model), n, *[a[0] for a in arrs], float(f_max),
+                                               float(step), ctypes.byref(err)))
+    return err.value

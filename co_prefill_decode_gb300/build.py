@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcf.so")
-SOURCES = ["engine.cu", "gemm.cu", "decode_attn.cu", "prefill_attn.cu", "rowops.cu", "decode_noalloc.cu"]
+SOURCES = ["engine.cu", "gemm.cu", "decode_attn.cu", "prefill_attn.cu", "rowops.cu", "decode_noalloc.cu",
+           "latency.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
@@ -44,7 +45,7 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = Fals
     jobs = []
     for src in SOURCES:
         sp = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         if force or _newer([sp] + headers, obj):
             cmd = [cc, *ARCH, *FLAGS, "-c", sp, "-o", obj]
             if ptxas_verbose:
@@ -65,7 +66,7 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = Fals
                 failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
     if force or jobs or _newer(objs, LIB):
         cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)

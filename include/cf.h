@@ -322,6 +322,69 @@ int cf_calibration_points(cf_engine* e, int* sms, float* ms, int cap);
 cf_status cf_get_phase_times(cf_engine* e, float* ms, int n, int* steps);
 long long cf_launch_count(cf_engine* e);
 
+/* ---- Iteration-latency estimator --------------------------------------
+ * ConfluxServe §6.2 "Latency Modeling and Estimation" (Eq. 2-6) with the
+ * base latency functions of App. D (Eq. 7-11).  Host code only: these calls
+ * touch no GPU, hold no state and are safe from any thread.  Times come out
+ * in the unit the coefficients were fitted in.
+ *
+ * Per iteration over L layers and N ranks:
+ *   T_iter = L (T_GEMM + T_ATTN)                                  (Eq. 2)
+ *   T_GEMM = f_GEMM(max_r (n_p^r + n_d^r))                        (Eq. 3)
+ *   T_ATTN = max{beta T_P, alpha T_D}                             (Eq. 4)
+ *   T_D    = max over ranks holding decodes of f_D(sum_i c_i)     (Eq. 5)
+ *   T_P    = f_comm(max_r n_p^r) + f_P((1/N) sum_i W_i)           (Eq. 6)
+ *   W_i    = l_i (c_i + (l_i + 1) / 2)                            (Eq. 9)
+ * with every f linear (Eq. 7, 8, 10, 11).  A path with no work takes no
+ * time (T_D = 0 without decodes, T_P = 0 without chunks, T_GEMM = 0 without
+ * tokens); f_comm is added only when N > 1. */
+typedef struct {
+  double gamma, gamma0;     /* f_GEMM(n) = gamma n + gamma0, n rank-local tokens (Eq. 7) */
+  double a_d, a_d0;         /* f_D(W) = a_d W + a_d0, W = sum of decode contexts (Eq. 8) */
+  double a_p, a_p0;         /* f_P(W) = a_p W + a_p0, W per-rank chunk workload (Eq. 10) */
+  double a_comm, a_comm0;   /* f_comm(n) = a_comm n + a_comm0, n largest shard (Eq. 11)  */
+  double alpha, beta;       /* contention factors of the decode / prefill path (Eq. 4)  */
+} cf_latency_model;
+
+typedef struct {
+  long long n_prefill;      /* n_p^r: prefill tokens assigned to rank r                 */
+  long long n_decode;       /* n_d^r: decode requests resident on rank r                */
+  double ctx_sum;           /* sum of c_i over rank r's resident decodes                */
+} cf_rank_load;
+
+typedef struct {
+  double t_iter, t_gemm, t_attn, t_prefill, t_decode;
+} cf_latency_parts;
+
+/* Predicts one iteration.  ranks: host [n_ranks]; chunk_len / chunk_ctx:
+ * host [n_chunks], the scheduled chunks' l_i and processed context c_i
+ * (chunks of length 0 are ignored).  Returns CF_ERR_INVALID_ARG for a null
+ * pointer, n_ranks < 1, a negative count or length, or a non-finite
+ * coefficient or context sum; *out is then left untouched. */
+cf_status cf_latency_predict(const cf_latency_model* m, int n_ranks, const cf_rank_load* ranks, int n_chunks,
+                             const long long* chunk_len, const long long* chunk_ctx, int n_layers,
+                             cf_latency_parts* out);
+
+/* Ordinary least-squares line y ~ slope x + intercept over n host points
+ * (App. D: each base function is fitted from offline profiles).
+ * CF_ERR_INVALID_ARG if n < 2, all x are equal or a value is not finite. */
+cf_status cf_latency_fit_line(const double* x, const double* y, int n, double* slope, double* intercept);
+
+/* Calibrates the contention factors of Eq. 4 on n co-batched profiles
+ * (App. D "Fitting"): for every pair (alpha, beta) on the grid
+ * {1, 1 + step, 1 + 2 step, ...} <= f_max, scores the mean absolute
+ * percentage error of t_gemm[i] + max(beta t_prefill[i], alpha t_decode[i])
+ * against t_meas[i] (the accuracy measure of ConfluxServe §8.4), and keeps
+ * the first minimum in (alpha, beta) order.  The inputs are host [n]:
+ * the fitted f_GEMM, f_P and f_D of each batch (0 for an absent path) and
+ * its measured time.  Writes m->alpha, m->beta and, if mape != NULL, the
+ * minimum in percent; the other fields of *m are left as they are.
+ * CF_ERR_INVALID_ARG for n < 1, step <= 0, f_max < 1, more than 100001 grid
+ * points per factor, a zero measured time or a non-finite value. */
+cf_status cf_latency_calibrate(cf_latency_model* m, int n, const double* t_gemm, const double* t_prefill,
+                               const double* t_decode, const double* t_meas, double f_max, double step,
+                               double* mape);
+
 #ifdef __cplusplus
 }
 #endif

@@ -50,7 +50,9 @@ def test_struct_layouts_match_header():
     # field order of the structs in cf.h
     src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     for struct, cls in (("cf_config", cf.cf_config), ("cf_weights", cf.cf_weights),
-                        ("cf_kv_pool", cf.cf_kv_pool), ("cf_batch", cf.cf_batch)):
+                        ("cf_kv_pool", cf.cf_kv_pool), ("cf_batch", cf.cf_batch),
+                        ("cf_latency_model", cf.cf_latency_model), ("cf_rank_load", cf.cf_rank_load),
+                        ("cf_latency_parts", cf.cf_latency_parts)):
         body = re.search(r"typedef struct \{([^{}]*?)\}\s*" + struct + ";", src).group(1)
         fields = re.findall(r"\**\s*(\w+)\s*(?:,|;)", body)
         assert [f[0] for f in cls._fields_] == fields, struct
