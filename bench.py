@@ -469,6 +469,175 @@ def run_kernel_case(args):
     return {"kernel_case": which, "ok": True}
 
 
+# ------------------------------------------------------------------ latency estimator
+# Table 4 of ConfluxServe (§8.4), measured on H100: estimator MAPE per model.
+PAGES_ESTIMATOR_MAPE = {"l8b": ("Llama-8B", 4.4), "q14b": ("Qwen-14B", 4.8), "q32b": ("Qwen-32B", 4.1)}
+LINEAR_PHASES = ("rmsnorm", "qkv", "oproj", "rmsnorm2", "gateup", "down")
+
+
+def run_estimator(args):
+    """Fits the iteration-latency estimator of ConfluxServe (§6.2 Eq. 2-6,
+    App. D Eq. 7-10) for one layer on this GPU and measures its accuracy the
+    way §8.4 does: MAPE over random heterogeneous iterations.
+
+    1. Profiles in isolation (the engine's per-phase CUDA events): the
+       shared linear region over a grid of token counts n (f_GEMM), the
+       attention region of decode-only iterations against W = sum c_i (f_D)
+       and of prefill-only iterations against W = l (c + (l+1)/2) (f_P).
+    2. Calibrates alpha, beta on co-batched iterations (whole-step time,
+       no profiling events).
+    3. Predicts and measures a second, independent set of co-batched
+       iterations; reports the MAPE.  One GPU: f_comm = 0, N = 1.
+    Every fit, calibration and prediction goes through the library's
+    estimator (cf_latency_fit_line / _calibrate / _predict)."""
+    import numpy as np
+    import torch
+
+    import co_prefill_decode_gb300 as cf
+    import workload as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    ps = 16
+    t_max = wl.EST_CHUNK[1] + wl.EST_DECODES[1]
+    pages_dec = -(-(wl.EST_CONTEXT[1] + 1) // ps)
+    pages_pre = -(-(wl.EST_CONTEXT[1] + wl.EST_CHUNK[1]) // ps)
+    n_dec_max = wl.EST_DECODES[1]
+    num_pages = n_dec_max * pages_dec + pages_pre
+    lines = []
+    for name in args.estimator.split(","):
+        w = wl.WORKLOADS[name]
+        s = w.shape
+        g = torch.Generator(device=dev).manual_seed(args.seed)
+        kp = torch.empty((num_pages, s.n_kv_heads, ps, s.head_dim), dtype=torch.bfloat16, device=dev)
+        vp = torch.empty_like(kp)
+        for t in (kp, vp):
+            t.normal_(generator=g)
+        perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(args.seed)).to(torch.int32)
+        dec_pages = perm[:n_dec_max * pages_dec].view(n_dec_max, pages_dec).contiguous().to(dev)
+        pre_pages = perm[n_dec_max * pages_dec:].contiguous().to(dev)
+        x = torch.randn(t_max, s.hidden, generator=g, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(x)
+        W = wl.make_weights(w, args.seed, "cuda", unit_gains=True)
+        eng = cf.Engine(cf.make_config(s, t_max, n_dec_max, args.decode_sms), W)
+        pool = cf.pool_of(kp, vp)
+
+        def run(it, reps, profile):
+            l, cp, ctx = it
+            nd = len(ctx)
+            dctx = torch.tensor(list(ctx) or [0], dtype=torch.int32, device=dev)
+            b = cf.batch_of(nd, dctx, dec_pages, l, cp, pre_pages)
+            T = l + nd
+            eng.cf_layer_step(b, x[:T], out[:T], pool, stream)          # warm-up
+            if profile:
+                eng.cf_set_profiling(True)
+                eng.cf_get_phase_times()
+                for _ in range(reps):
+                    eng.cf_layer_step(b, x[:T], out[:T], pool, stream)
+                torch.cuda.synchronize()
+                ph, n = eng.cf_get_phase_times()
+                eng.cf_set_profiling(False)
+                return {k: v / n for k, v in ph.items()}
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for e0, e1 in evs:
+                e0.record(stream)
+                eng.cf_layer_step(b, x[:T], out[:T], pool, stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            return float(np.median([e0.elapsed_time(e1) for e0, e1 in evs]))
+
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.3)
+        clocks.mark("t0")
+        t_start = time.perf_counter()
+        # 1. isolated profiles
+        grid = sorted({32, 64, 128, 256, 384, 512, 768} | set(range(1024, t_max, 512)) | {t_max})
+        n_gemm, t_gemm_prof = [], []
+        for n in grid:
+            ph = run((n, 0, ()), args.est_reps, True)
+            n_gemm.append(n)
+            t_gemm_prof.append(sum(ph[k] for k in LINEAR_PHASES))
+        dec_iso = wl.estimator_batches(args.seed, args.est_profile, "decode")
+        pre_iso = wl.estimator_batches(args.seed, args.est_profile, "prefill")
+        wd, td = [], []
+        for it in dec_iso:
+            wd.append(float(sum(it[2])))
+            td.append(run(it, args.est_reps, True)["fork"])
+        wp, tp = [], []
+        for it in pre_iso:
+            wp.append(float(it[0]) * (it[1] + (it[0] + 1) / 2.0))
+            tp.append(run(it, args.est_reps, True)["fork"])
+        model = cf.cf_latency_model()
+        model.gamma, model.gamma0 = cf.cf_latency_fit_line(n_gemm, t_gemm_prof)
+        model.a_d, model.a_d0 = cf.cf_latency_fit_line(wd, td)
+        model.a_p, model.a_p0 = cf.cf_latency_fit_line(wp, tp)
+
+        def parts(it):
+            l, cp, ctx = it
+            return cf.cf_latency_predict(model, [(l, len(ctx), float(sum(ctx)))], [(l, cp)] if l else [], 1)
+
+        # 2. contention factors from co-batched iterations (plain step time)
+        cal = wl.estimator_batches(args.seed, args.est_calibrate, "calibrate")
+        cal_meas = [run(it, args.est_reps, False) for it in cal]
+        cal_parts = [parts(it) for it in cal]
+        calib_mape = cf.cf_latency_calibrate(model, [p["t_gemm"] for p in cal_parts],
+                                             [p["t_prefill"] for p in cal_parts],
+                                             [p["t_decode"] for p in cal_parts], cal_meas, 4.0, 0.005)
+        # 3. validation on an independent draw
+        val = wl.estimator_batches(args.seed, args.est_validate, "validate")
+        meas = np.array([run(it, args.est_reps, False) for it in val])
+        pred = np.array([parts(it)["t_iter"] for it in val])
+        ape = np.abs(pred - meas) / meas * 100.0
+        # the same iterations without contention factors (alpha = beta = 1)
+        m1 = cf.cf_latency_model(**{f: getattr(model, f) for f, _ in cf.cf_latency_model._fields_})
+        m1.alpha = m1.beta = 1.0
+        pred1 = np.array([cf.cf_latency_predict(m1, [(l, len(c), float(sum(c)))], [(l, cp)], 1)["t_iter"]
+                          for l, cp, c in val])
+        clocks.mark("t1")
+        clocks.stop()
+        page_model, page_mape = PAGES_ESTIMATOR_MAPE.get(name, (None, None))
+
+        def r2(xs, ys, a, a0):
+            xs, ys = np.asarray(xs), np.asarray(ys)
+            res = ys - (a * xs + a0)
+            return float(1.0 - (res ** 2).sum() / ((ys - ys.mean()) ** 2).sum())
+
+        line = {
+            "estimator": name, "workload": f"{name}: {s.n_q_heads}/{s.n_kv_heads} heads, H {s.hidden}, "
+                                          f"F {s.ffn_dim}; one layer, one GPU",
+            "mape_pct": round(float(ape.mean()), 3), "n_validate": len(val),
+            "ape_p50_pct": round(float(np.percentile(ape, 50)), 3),
+            "ape_p90_pct": round(float(np.percentile(ape, 90)), 3), "ape_max_pct": round(float(ape.max()), 3),
+            "mape_alpha_beta_1_pct": round(float((np.abs(pred1 - meas) / meas).mean() * 100), 3),
+            "calibrate": {"n": len(cal), "mape_pct": round(calib_mape, 3)},
+            "coeffs_ms": {f: getattr(model, f) for f, _ in cf.cf_latency_model._fields_},
+            "fit_r2": {"gemm": r2(n_gemm, t_gemm_prof, model.gamma, model.gamma0),
+                       "decode": r2(wd, td, model.a_d, model.a_d0), "prefill": r2(wp, tp, model.a_p, model.a_p0)},
+            "profiles": {"gemm_points": len(n_gemm), "decode_points": len(wd), "prefill_points": len(wp),
+                         "reps": args.est_reps},
+            "ranges": {"chunk": wl.EST_CHUNK, "decodes": wl.EST_DECODES, "context": wl.EST_CONTEXT},
+            "step_ms": {"min": round(float(meas.min()), 4), "median": round(float(np.median(meas)), 4),
+                        "max": round(float(meas.max()), 4)},
+            "pages": {"model": page_model, "mape_pct": page_mape, "hardware": "H100 (context, not a target)"},
+            "clocks": clocks.summary(), "seconds": round(time.perf_counter() - t_start, 1),
+        }
+        if args.estimator_out:
+            with open(args.estimator_out, "a") as f:
+                f.write(json.dumps({"estimator": name, "validate": [
+                    {"l": l, "c_p": cp, "n_d": len(c), "ctx_sum": int(sum(c)), "meas_ms": float(mm),
+                     "pred_ms": float(pp)} for (l, cp, c), mm, pp in zip(val, meas, pred)],
+                    "gemm": list(zip(n_gemm, t_gemm_prof)), "decode": list(zip(wd, td)),
+                    "prefill": list(zip(wp, tp))}) + "\n")
+        lines.append(line)
+        eng.close()
+        del kp, vp, x, out, W
+        torch.cuda.empty_cache()
+    return lines
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
     """The reference arm: the fp64 oracle timed on the host cores, each step a
@@ -517,11 +686,23 @@ def main(argv=None):
                     help="replay the linear segments of the step as CUDA graphs (1) or launch eagerly (0)")
     ap.add_argument("--kernel", choices=["decode", "prefill", "gemm"], default=None,
                     help="run one small launch of one kernel (for ncu) instead of the benchmark")
+    ap.add_argument("--estimator", default=None,
+                    help="fit and validate the iteration-latency estimator for these workloads "
+                         "(comma-separated, e.g. l8b,q14b,q32b) instead of the benchmark")
+    ap.add_argument("--est-reps", type=int, default=3)
+    ap.add_argument("--est-profile", type=int, default=40)
+    ap.add_argument("--est-calibrate", type=int, default=50)
+    ap.add_argument("--est-validate", type=int, default=200)
+    ap.add_argument("--estimator-out", default=None, help="append per-iteration records (JSON lines) here")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.kernel:
         print(json.dumps(run_kernel_case(args)))
+        return
+    if args.estimator:
+        for line in run_estimator(args):
+            print(json.dumps(line), flush=True)
         return
     rank, world, local, pg = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -398,3 +398,30 @@ def test_layer_step_graphs_match_eager(cf):
     assert torch.equal(graph2, eager2)
     assert not torch.equal(eager2, eager)
     S.eng.cf_set_graphs(False)
+
+
+@pytest.mark.gpu
+def test_latency_estimator_fits_and_predicts_through_the_library(cf, tmp_path):
+    # the estimator study of bench.py on a small sample: isolated profiles ->
+    # fitted lines -> calibrated contention factors -> predictions; the
+    # library's predictions on the measured coefficients equal the oracle's
+    import argparse
+    import json
+
+    import bench
+    from oracle import latency as OL
+    out = tmp_path / "est.jsonl"
+    args = argparse.Namespace(estimator="tiny", seed=0, decode_sms=0, est_reps=1, est_profile=5,
+                              est_calibrate=5, est_validate=8, estimator_out=str(out))
+    (line,) = bench.run_estimator(args)
+    c = line["coeffs_ms"]
+    assert c["gamma"] > 0 and c["a_d"] > 0 and c["a_p"] > 0
+    assert 1.0 <= c["alpha"] <= 4.0 and 1.0 <= c["beta"] <= 4.0
+    assert np.isfinite(line["mape_pct"]) and line["n_validate"] == 8
+    m = OL.LatencyModel(**c)
+    rec = json.loads(out.read_text().splitlines()[0])
+    for v, it in zip(rec["validate"], wl.estimator_batches(0, 8, "validate")):
+        assert (v["l"], v["c_p"], v["n_d"], v["ctx_sum"]) == (it[0], it[1], len(it[2]), sum(it[2]))
+        ranks, chunks = OL.one_gpu(*it)
+        assert v["pred_ms"] == pytest.approx(OL.t_iter(m, ranks, chunks)["t_iter"], rel=1e-12)
+        assert v["meas_ms"] > 0

@@ -261,3 +261,34 @@ def make_pools(w: Workload, batch: Batch, seed: int = 0, device="cpu") -> Tuple[
                 pool[int(pages[full]), :, :rem] = vals[full * ps:].transpose(0, 1)
         pools.append(pool)
     return pools[0], pools[1]
+
+
+# --------------------------------------------------------------------------
+# Random iterations for the latency-estimator study
+# --------------------------------------------------------------------------
+# Ranges of ConfluxServe §8.4 ("Latency-Estimator Accuracy"): prefill chunks
+# of 32 to 10K tokens, decode batches of 1 to 128 requests, context lengths
+# of 1K to 16K tokens (read as: every decode's c_j and the chunk's processed
+# prefix c_p, each uniform over the range; K = 1024).
+EST_CHUNK = (32, 10240)
+EST_DECODES = (1, 128)
+EST_CONTEXT = (1024, 16384)
+_EST_KINDS = {"validate": 1, "calibrate": 2, "decode": 3, "prefill": 4}
+
+
+def estimator_batches(seed: int, n: int, kind: str = "validate"):
+    """``n`` random iterations as (l, c_p, dec_ctx tuple).
+
+    ``validate`` / ``calibrate``: co-batched iterations (a chunk and decodes)
+    from two independent streams; ``decode``: decodes only (l = 0);
+    ``prefill``: a chunk only.  Lengths are uniform integers over the ranges
+    above, inclusive."""
+    rng = np.random.default_rng([int(seed), _EST_KINDS[kind]])
+    out = []
+    for _ in range(n):
+        l = int(rng.integers(EST_CHUNK[0], EST_CHUNK[1] + 1)) if kind != "decode" else 0
+        c_p = int(rng.integers(EST_CONTEXT[0], EST_CONTEXT[1] + 1)) if l else 0
+        nd = int(rng.integers(EST_DECODES[0], EST_DECODES[1] + 1)) if kind != "prefill" else 0
+        ctx = tuple(int(c) for c in rng.integers(EST_CONTEXT[0], EST_CONTEXT[1] + 1, size=nd))
+        out.append((l, c_p, ctx))
+    return out
