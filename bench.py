@@ -473,6 +473,12 @@ def run_kernel_case(args):
 # Table 4 of ConfluxServe (§8.4), measured on H100: estimator MAPE per model.
 PAGES_ESTIMATOR_MAPE = {"l8b": ("Llama-8B", 4.4), "q14b": ("Qwen-14B", 4.8), "q32b": ("Qwen-32B", 4.1)}
 LINEAR_PHASES = ("rmsnorm", "qkv", "oproj", "rmsnorm2", "gateup", "down")
+# transformer layers of the models whose layer shapes the workloads take
+MODEL_LAYERS = {"l8b": 32, "q14b": 40, "q32b": 64}
+# ConfluxServe §3.1 (Fig. 3c), H100, Qwen3-14B with 16 decodes at 8K context:
+# about 1K prefill tokens fit a 50 ms TBT and about 2.2K fit 100 ms
+PAGES_TBT_CHUNK = {"q14b": {50.0: 1000, 100.0: 2200}}
+TBT_QUANTUM = 128    # alignment quantum of the level: one GEMM row tile
 
 
 def run_estimator(args):
@@ -596,6 +602,22 @@ def run_estimator(args):
         m1.alpha = m1.beta = 1.0
         pred1 = np.array([cf.cf_latency_predict(m1, [(l, len(c), float(sum(c)))], [(l, cp)], 1)["t_iter"]
                           for l, cp, c in val])
+        # 4. the dispatcher on one GPU (Algorithm 2 with N = 1): the largest
+        # TBT-safe chunk for a new prompt next to 16 decodes at 8K, over
+        # the model's layers, then that iteration measured
+        tbt = []
+        if name in MODEL_LAYERS:
+            layers = MODEL_LAYERS[name]
+            ctx16 = (8192,) * 16
+            for tau in (50.0, 100.0):
+                r = cf.cf_waterfill_dispatch(model, layers, tau, TBT_QUANTUM, [len(ctx16)], [float(sum(ctx16))],
+                                             [0], [], (t_max - len(ctx16), 0))
+                l = int(r["chunk"])
+                meas_layer = run((l, 0, ctx16), args.est_reps, False) if l > 0 else None
+                tbt.append({"tbt_ms": tau, "layers": layers, "chunk": l, "capped": l == t_max - len(ctx16),
+                            "pred_ms": round(r["t_iter"], 3),
+                            "meas_ms": round(layers * meas_layer, 3) if meas_layer else None,
+                            "pages_h100_chunk": PAGES_TBT_CHUNK.get(name, {}).get(tau)})
         clocks.mark("t1")
         clocks.stop()
         page_model, page_mape = PAGES_ESTIMATOR_MAPE.get(name, (None, None))
@@ -622,6 +644,7 @@ def run_estimator(args):
             "step_ms": {"min": round(float(meas.min()), 4), "median": round(float(np.median(meas)), 4),
                         "max": round(float(meas.max()), 4)},
             "pages": {"model": page_model, "mape_pct": page_mape, "hardware": "H100 (context, not a target)"},
+            "tbt_chunk": {"decodes": "16 @ 8192", "quantum": TBT_QUANTUM, "layers_only": True, "cases": tbt},
             "clocks": clocks.summary(), "seconds": round(time.perf_counter() - t_start, 1),
         }
         if args.estimator_out:

@@ -29,7 +29,8 @@ EXPORTS = (
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
     "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
-    "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate",
+    "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate", "cf_waterfill_dispatch",
+    "cf_waterfill_assign",
 )
 
 
@@ -72,6 +73,18 @@ class cf_rank_load(ctypes.Structure):
 
 class cf_latency_parts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_double) for n in ("t_iter", "t_gemm", "t_attn", "t_prefill", "t_decode")]
+
+
+class cf_dispatch_state(ctypes.Structure):
+    _fields_ = [("n_ranks", ctypes.c_int), ("n_decode", ctypes.POINTER(ctypes.c_longlong)),
+                ("ctx_sum", ctypes.POINTER(ctypes.c_double)), ("n_prefill", ctypes.POINTER(ctypes.c_longlong)),
+                ("n_chunks", ctypes.c_int), ("chunk_len", ctypes.POINTER(ctypes.c_longlong)),
+                ("chunk_ctx", ctypes.POINTER(ctypes.c_longlong))]
+
+
+class cf_dispatch_result(ctypes.Structure):
+    _fields_ = [("n_target", ctypes.c_longlong), ("budget", ctypes.c_longlong), ("chunk", ctypes.c_longlong),
+                ("feasible", ctypes.c_int), ("t_iter", ctypes.c_double)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -121,6 +134,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
         "cf_latency_calibrate": (I, [ctypes.POINTER(cf_latency_model), I] + [ctypes.POINTER(ctypes.c_double)] * 4
                                  + [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]),
+        "cf_waterfill_dispatch": (I, [ctypes.POINTER(cf_latency_model), I, ctypes.c_double, L,
+                                      ctypes.POINTER(cf_dispatch_state), L, L, ctypes.POINTER(cf_dispatch_result),
+                                      ctypes.POINTER(L)]),
+        "cf_waterfill_assign": (I, [ctypes.POINTER(L), I, L, L, ctypes.POINTER(L)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -385,3 +402,40 @@ def cf_latency_calibrate(model: cf_latency_model, t_gemm, t_prefill, t_decode, t
     _check(lib, None, lib.cf_latency_calibrate(ctypes.byref(model), n, *[a[0] for a in arrs], float(f_max),
                                                float(step), ctypes.byref(err)))
     return err.value
+
+
+def _longs(v):
+    v = [int(x) for x in v]
+    return (ctypes.c_longlong * max(len(v), 1))(*v)
+
+
+def cf_waterfill_dispatch(model: cf_latency_model, n_layers: int, tbt_slo: float, quantum: int, n_decode,
+                          ctx_sum, n_prefill, chunks=(), request=None) -> Dict[str, object]:
+    """Algorithm 2 over len(n_decode) ranks.  chunks: scheduled [(l_j, c_j)];
+    request: (m_i, c_i) or None (budget only).  Returns n_target, budget,
+    chunk, feasible, t_iter and assign (A_i per rank)."""
+    lib = load_library()
+    n = len(n_decode)
+    if len(ctx_sum) != n or len(n_prefill) != n:
+        raise ValueError("per-rank lists differ in length")
+    nd, cs, npf = _longs(n_decode), _doubles(ctx_sum)[0], _longs(n_prefill)
+    cl, cc = _longs([l for l, _ in chunks]), _longs([c for _, c in chunks])
+    st = cf_dispatch_state(n, nd, cs, npf, len(chunks), cl, cc)
+    out = cf_dispatch_result()
+    give = (ctypes.c_longlong * max(n, 1))()
+    m_i, c_i = (-1, 0) if request is None else (int(request[0]), int(request[1]))
+    _check(lib, None, lib.cf_waterfill_dispatch(ctypes.byref(model), int(n_layers), float(tbt_slo), int(quantum),
+                                                ctypes.byref(st), m_i, c_i, ctypes.byref(out), give))
+    res = {n_: getattr(out, n_) for n_, _ in cf_dispatch_result._fields_}
+    res["feasible"] = bool(res["feasible"])
+    res["assign"] = [int(give[r]) for r in range(n)]
+    return res
+
+
+def cf_waterfill_assign(loads, tokens: int, n_target: int):
+    """WaterfillAssign alone: tokens per rank."""
+    lib = load_library()
+    n = len(loads)
+    give = (ctypes.c_longlong * max(n, 1))()
+    _check(lib, None, lib.cf_waterfill_assign(_longs(loads), n, int(tokens), int(n_target), give))
+    return [int(give[r]) for r in range(n)]

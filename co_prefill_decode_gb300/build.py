@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcf.so")
 SOURCES = ["engine.cu", "gemm.cu", "decode_attn.cu", "prefill_attn.cu", "rowops.cu", "decode_noalloc.cu",
-           "latency.cpp"]
+           "latency.cpp", "dispatch.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

@@ -385,6 +385,65 @@ cf_status cf_latency_calibrate(cf_latency_model* m, int n, const double* t_gemm,
                                const double* t_decode, const double* t_meas, double f_max, double step,
                                double* mape);
 
+/* ---- Waterfill prefill dispatch ----------------------------------------
+ * ConfluxServe §6.3 "Prefill: waterfill dispatch" and App. E Algorithm 2.
+ * Host code only (no GPU, no state).  Given the decode state and the prefill
+ * already assigned this iteration, finds the largest combined-load level
+ * n_target (a multiple of the alignment quantum q) whose estimated
+ * iteration latency (cf_latency_predict) stays within the TBT SLO, the
+ * budget B = sum_r max{0, n_target - n_d^r - n_p^r}, and for a request
+ * with m_i prefill tokens left the chunk l_i = min{m_i, B} and its per-rank
+ * split A_i.
+ *
+ * Readings of what the pages leave open:
+ * - A level n is feasible if the iteration it would run is within the SLO:
+ *   with a request, rank r carries n_p^r + A_i^r(n) prefill tokens and the
+ *   chunk (l_i(n), c_i) joins the scheduled chunks; without one, every rank
+ *   is filled to n by tokens that count for Eq. 3 and f_comm but carry no
+ *   attention workload.
+ * - Search: level 0 first (if even that is over the SLO, nothing fits:
+ *   feasible = 0, B = 0).  With a request the search range ends at the
+ *   first level whose budget covers m_i; without one its end is found by
+ *   doubling (capped at 2^40 tokens).  Bisection then finds the largest
+ *   feasible multiple of q.
+ * - Water-filling (cf_waterfill_assign): the tokens raise the lowest loads
+ *   first to a common level w <= n_target; tokens left over after the last
+ *   whole level go one each to the ranks standing at w, lowest rank index
+ *   first. */
+typedef struct {
+  int n_ranks;
+  const long long* n_decode;    /* host [n_ranks]: n_d^r                                 */
+  const double* ctx_sum;        /* host [n_ranks]: sum of the resident decodes' c_i      */
+  const long long* n_prefill;   /* host [n_ranks]: n_p^r of the existing assignment A_p  */
+  int n_chunks;                 /* prefill chunks P already scheduled this iteration     */
+  const long long* chunk_len;   /* host [n_chunks]: their l_j                            */
+  const long long* chunk_ctx;   /* host [n_chunks]: their processed context c_j          */
+} cf_dispatch_state;
+
+typedef struct {
+  long long n_target;           /* the level (0 when nothing fits)                       */
+  long long budget;             /* B at that level                                       */
+  long long chunk;              /* l_i (0 without a request)                             */
+  int feasible;                 /* 0: even level 0 exceeds the SLO                       */
+  double t_iter;                /* estimated latency of the iteration at n_target        */
+} cf_dispatch_result;
+
+/* remaining < 0 asks for the budget only (Algorithm 2 with no request);
+ * otherwise remaining = m_i and context = c_i of the request.  assign:
+ * host [n_ranks] receives A_i (zeros without a request) or may be NULL.
+ * CF_ERR_INVALID_ARG for a null pointer, n_ranks < 1, quantum < 1, a
+ * negative count, a NaN SLO or an invalid model (as cf_latency_predict). */
+cf_status cf_waterfill_dispatch(const cf_latency_model* m, int n_layers, double tbt_slo, long long quantum,
+                                const cf_dispatch_state* s, long long remaining, long long context,
+                                cf_dispatch_result* out, long long* assign);
+
+/* WaterfillAssign alone: splits `tokens` over ranks with combined loads
+ * loads[n_ranks] toward n_target; give: host [n_ranks].
+ * CF_ERR_INVALID_ARG if tokens exceed sum_r max{0, n_target - loads[r]} or a
+ * load or tokens is negative. */
+cf_status cf_waterfill_assign(const long long* loads, int n_ranks, long long tokens, long long n_target,
+                              long long* give);
+
 #ifdef __cplusplus
 }
 #endif

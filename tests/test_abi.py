@@ -52,7 +52,8 @@ def test_struct_layouts_match_header():
     for struct, cls in (("cf_config", cf.cf_config), ("cf_weights", cf.cf_weights),
                         ("cf_kv_pool", cf.cf_kv_pool), ("cf_batch", cf.cf_batch),
                         ("cf_latency_model", cf.cf_latency_model), ("cf_rank_load", cf.cf_rank_load),
-                        ("cf_latency_parts", cf.cf_latency_parts)):
+                        ("cf_latency_parts", cf.cf_latency_parts), ("cf_dispatch_state", cf.cf_dispatch_state),
+                        ("cf_dispatch_result", cf.cf_dispatch_result)):
         body = re.search(r"typedef struct \{([^{}]*?)\}\s*" + struct + ";", src).group(1)
         fields = re.findall(r"\**\s*(\w+)\s*(?:,|;)", body)
         assert [f[0] for f in cls._fields_] == fields, struct
