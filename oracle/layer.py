@@ -226,18 +226,20 @@ def layer_step(x: np.ndarray, W: LayerWeights64, shape, batch, k_pool, v_pool,
                round_bf16: bool = True, rows: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
     """One co-batched layer step.
 
-    x [T, H] is the stacked token matrix, rows ordered [prefill chunk; decodes]
-    (ConfluxServe §4, Fig. 7).  ``k_pool``/``v_pool`` hold the cache BEFORE the
+    x [T, H] is the stacked token matrix, rows ordered [prefill chunks; decodes]
+    (ConfluxServe §4, Fig. 7); the chunks of several requests (the batch P of
+    ConfluxServe §6.2 Eq. 6) follow one another, chunk i's row r sitting at
+    position c_i + r of its own request.  ``k_pool``/``v_pool`` hold the cache BEFORE the
     step (torch or numpy, [num_pages, Hkv, ps, d]); they are not modified.
 
     Steps (ConfluxServe Fig. 1 and §4; Decode Token Parallelism §4.3):
       1. xn = RMSNorm(x) g_attn
       2. qkv = xn W_qkv^T, split Q | K | V heads (Decode Token Parallelism §4.4)
       3. optional per-head RMSNorm of q and k over d (QK-norm)
-      4. RoPE at each row's position (prefill row i: c_p + i; decode j: c_j)
+      4. RoPE at each row's position (chunk row i: c_i + i; decode j: c_j)
       5. append k, v at slot(position) of the row's request
-      6. attention: prefill rows causal over prefix + chunk, decode rows over
-         their own c_j + 1 keys
+      6. attention: each chunk's rows causal over its own request's prefix +
+         chunk, decode rows over their own c_j + 1 keys
       7. h = x + O W_o^T
       8. hn = RMSNorm(h) g_ffn
       9. out = h + (silu(hn W_gate^T) * (hn W_up^T)) W_down^T
@@ -250,17 +252,29 @@ def layer_step(x: np.ndarray, W: LayerWeights64, shape, batch, k_pool, v_pool,
     """
     s = shape
     Hq, Hkv, d, ps = s.n_q_heads, s.n_kv_heads, s.head_dim, batch.page_size
-    l, cp, nd = batch.prefill_len, batch.prefill_prefix, batch.n_decode
-    T = l + nd
+    chunks = list(batch.chunks)            # (l_i, c_i, page ids), stacked in this order
+    nd = batch.n_decode
+    P = sum(c[0] for c in chunks)          # prefill rows
+    T = P + nd
     R = bf16_round if round_bf16 else (lambda a: a)
     rows = np.arange(T) if rows is None else np.asarray(sorted(set(int(r) for r in rows)))
-    pre_rows = rows[rows < l]
-    dec_rows = rows[rows >= l]
-    # rows whose q/k/v are needed: every prefill row up to the last selected one
-    # (its keys are visible to later chunk rows), plus the selected decode rows.
-    need_pre = np.arange(int(pre_rows.max()) + 1) if len(pre_rows) else np.arange(0)
+    pre_rows = rows[rows < P]
+    dec_rows = rows[rows >= P]
+    # rows whose q/k/v are needed: in each chunk every row up to its last
+    # selected one (its keys are visible to later rows of the same chunk),
+    # plus the selected decode rows.
+    segs, need_parts, pos_parts = [], [], []
+    r0 = 0
+    for l_i, c_i, pages_i in chunks:
+        sel = pre_rows[(pre_rows >= r0) & (pre_rows < r0 + l_i)]
+        n_i = int(sel.max()) - r0 + 1 if len(sel) else 0
+        segs.append((r0, l_i, c_i, pages_i, n_i, sel))
+        need_parts.append(r0 + np.arange(n_i))
+        pos_parts.append(c_i + np.arange(n_i))
+        r0 += l_i
+    need_pre = np.concatenate(need_parts) if need_parts else np.arange(0)
     need = np.concatenate([need_pre, dec_rows]).astype(np.int64)
-    pos = np.concatenate([cp + need_pre, batch.dec_ctx[dec_rows - l].astype(np.int64)])
+    pos = np.concatenate(pos_parts + [batch.dec_ctx[dec_rows - P].astype(np.int64)]).astype(np.int64)
 
     xs = x[need]
     xn = R(rmsnorm(xs, W.g_attn, s.rms_eps))
@@ -276,17 +290,22 @@ def layer_step(x: np.ndarray, W: LayerWeights64, shape, batch, k_pool, v_pool,
     v = R(v)
 
     attn = np.zeros((len(need), Hq, d))
-    npre = len(need_pre)
-    if npre:
-        # cached prefix followed by the chunk's own (appended) keys
-        Kc = gather_request_kv(k_pool, batch.pre_pages, cp, ps)
-        Vc = gather_request_kv(v_pool, batch.pre_pages, cp, ps)
-        K = np.concatenate([Kc, k[:npre]])
-        V = np.concatenate([Vc, v[:npre]])
-        sel = pre_rows  # only the selected prefill rows need attention
-        attn[sel] = attention(q[sel], K, V, cp + sel)
+    where_pre = []
+    off = 0                                # index of the chunk's first row in ``need``
+    for r0, l_i, c_i, pages_i, n_i, sel in segs:
+        if n_i:
+            # the request's cached prefix followed by the chunk's own (appended) keys
+            Kc = gather_request_kv(k_pool, pages_i, c_i, ps)
+            Vc = gather_request_kv(v_pool, pages_i, c_i, ps)
+            K = np.concatenate([Kc, k[off:off + n_i]])
+            V = np.concatenate([Vc, v[off:off + n_i]])
+            loc = sel - r0                 # only the selected rows need attention
+            attn[off + loc] = attention(q[off + loc], K, V, c_i + loc)
+            where_pre.append(off + loc)
+        off += n_i
+    npre = off
     for t, r in enumerate(dec_rows):
-        j = int(r) - l
+        j = int(r) - P
         c = int(batch.dec_ctx[j])
         Kc = gather_request_kv(k_pool, batch.dec_pages[j], c, ps)
         Vc = gather_request_kv(v_pool, batch.dec_pages[j], c, ps)
@@ -296,7 +315,7 @@ def layer_step(x: np.ndarray, W: LayerWeights64, shape, batch, k_pool, v_pool,
     attn = R(attn)
 
     # positions in ``need`` of the selected rows
-    where = np.concatenate([pre_rows, npre + np.arange(len(dec_rows))]).astype(np.int64)
+    where = np.concatenate(where_pre + [npre + np.arange(len(dec_rows))]).astype(np.int64)
     a_sel = attn[where].reshape(len(rows), Hq * d)
     h = x[rows] + a_sel @ W.w_o.T
     hn = R(rmsnorm(h, W.g_ffn, s.rms_eps))
@@ -306,10 +325,13 @@ def layer_step(x: np.ndarray, W: LayerWeights64, shape, batch, k_pool, v_pool,
     # slots written by the append, for the selected rows
     slots = []
     for r in rows:
-        if r < l:
-            slots.append(int(slot_of(batch.pre_pages, cp + r, ps)))
+        if r < P:
+            for r0, l_i, c_i, pages_i, _, _ in segs:
+                if r0 <= r < r0 + l_i:
+                    slots.append(int(slot_of(pages_i, c_i + int(r) - r0, ps)))
+                    break
         else:
-            j = int(r) - l
+            j = int(r) - P
             slots.append(int(slot_of(batch.dec_pages[j], int(batch.dec_ctx[j]), ps)))
     return {
         "rows": rows, "out": out, "h": h, "hn": hn, "act": act,

@@ -207,11 +207,20 @@ def test_slot_and_gather_match_contiguous_cache():
     assert changed.sum() == 2 * Hkv * d
 
 
+# several prefill chunks of different requests in one step (ConfluxServe
+# §6.2 Eq. 6: the scheduled prefill batch P), plus decodes
+TINY_MC = wl.Workload("tiny-mc", wl.TINY, 3, (5, 40, 200), 64, 128,
+                      more_chunks=((37, 0), (130, 300), (1, 17)), description="tiny, four chunks")
+
+
 def test_workload_pages_cover_each_request_once():
-    for name in ("tiny", "mix"):
+    for name in ("tiny", "mix", "mchunk"):
         w = wl.WORKLOADS[name]
         b = wl.make_batch(w)
-        used = list(b.pre_pages)
+        used = []
+        for l, c, p in b.chunks:
+            assert len(p) == (l + c + 15) // 16
+            used += list(p)
         for j in range(b.n_decode):
             npg = (int(b.dec_ctx[j]) + 1 + 15) // 16
             assert (b.dec_pages[j, :npg] >= 0).all() and (b.dec_pages[j, npg:] == -1).all()
@@ -232,6 +241,25 @@ def test_pool_generation_places_tokens_by_page_table():
         assert np.isfinite(Kg[:c]).all() and np.isnan(Kg[c]).all()
     Kp = oracle.gather_request_kv(kp, b.pre_pages, b.prefill_prefix + b.prefill_len, 16)
     assert np.isfinite(Kp[:b.prefill_prefix]).all() and np.isnan(Kp[b.prefill_prefix:]).all()
+    b = wl.make_batch(TINY_MC)
+    kp, vp = wl.make_pools(TINY_MC, b)
+    for l, c, p in b.chunks:
+        Kp = oracle.gather_request_kv(kp, p, c + l, 16)
+        assert np.isfinite(Kp[:c]).all() and np.isnan(Kp[c:]).all()
+
+
+def test_extra_chunks_leave_the_first_requests_draws_unchanged():
+    # the extra chunks' prefixes are drawn after every other request, so a
+    # one-chunk batch's cached KV, pages and x rows do not move
+    one = wl.Workload("one", wl.TINY, 3, (5, 40, 200), 64, 128)
+    b1, bm = wl.make_batch(one), wl.make_batch(TINY_MC)
+    assert np.array_equal(b1.dec_ctx, bm.dec_ctx)
+    k1, _ = wl.make_pools(one, b1)
+    km, _ = wl.make_pools(TINY_MC, bm)
+    for j in range(b1.n_decode):
+        c = int(b1.dec_ctx[j])
+        assert torch.equal(torch.as_tensor(oracle.gather_request_kv(k1, b1.dec_pages[j], c, 16)),
+                           torch.as_tensor(oracle.gather_request_kv(km, bm.dec_pages[j], c, 16)))
 
 
 # ------------------------------------------------------------------ layer
@@ -275,6 +303,38 @@ def test_layer_cobatched_rows_equal_separate_rows():
     dec = oracle.layer_step(x[l:], W, w.shape, b_dec, kp, vp)
     assert np.allclose(full["out"][:l], pre["out"], rtol=0, atol=0)
     assert np.allclose(full["out"][l:], dec["out"], rtol=0, atol=0)
+
+
+def test_multi_chunk_rows_equal_each_chunk_alone():
+    """Each chunk of a multi-chunk step (ConfluxServe §6.2 Eq. 6: several
+    requests' chunks in one iteration) computes exactly what it computes as
+    the only chunk of a step: same positions, own prefix, own pages; and the
+    decode rows are unaffected."""
+    w = TINY_MC
+    b = wl.make_batch(w)
+    x = oracle.to_f64(wl.make_x(w, b))
+    W = oracle.LayerWeights64.from_torch(wl.make_weights(w))
+    kp, vp = (oracle.to_f64(t) for t in wl.make_pools(w, b))
+    full = oracle.layer_step(x, W, w.shape, b, kp, vp)
+    assert full["out"].shape[0] == 64 + 37 + 130 + 1 + 3
+    r0 = 0
+    for l, c, p in b.chunks:
+        alone = wl.Batch(w, b.dec_ctx[:0], l, c, b.dec_pages[:0], p, b.num_pages)
+        r = oracle.layer_step(x[r0:r0 + l], W, w.shape, alone, kp, vp)
+        for key in ("out", "q", "k", "v", "attn", "slots"):
+            assert np.array_equal(full[key][r0:r0 + l], r[key]), key
+        # slot of chunk row i: position c + i through the chunk's own table
+        pos = c + np.arange(l)
+        assert np.array_equal(full["slots"][r0:r0 + l], p[pos // 16].astype(np.int64) * 16 + pos % 16)
+        r0 += l
+    dec = wl.Batch(w, b.dec_ctx, 0, 0, b.dec_pages, b.pre_pages[:0], b.num_pages)
+    r = oracle.layer_step(x[r0:], W, w.shape, dec, kp, vp)
+    assert np.array_equal(full["out"][r0:], r["out"])
+    # a row subset spanning several chunks matches the full step
+    rows = [0, 63, 64, 100, 101, 230, 231, 232, 234]
+    sub = oracle.layer_step(x, W, w.shape, b, kp, vp, rows=rows)
+    for key in ("out", "attn", "slots"):
+        assert np.array_equal(sub[key], full[key][rows]), key
 
 
 def _append_rows(r, b, kp, vp):

@@ -90,6 +90,9 @@ class Workload:
     pool_slack: float = 1.0                   # pool pages / pages needed
     lognormal: Tuple[float, float, int, int] = (6346.0, 0.86, 512, 32768)
     description: str = ""
+    # further prefill chunks (l_i, c_i) of other requests, stacked after the
+    # first chunk's rows (the batch P of ConfluxServe §6.2 Eq. 6 / Alg. 1)
+    more_chunks: Tuple[Tuple[int, int], ...] = ()
 
 
 LLAMA8B = LayerShape(4096, 32, 8, 128, 14336, 5.0e5, 1e-5, False)
@@ -112,6 +115,10 @@ WORKLOADS: Dict[str, Workload] = {
     "q32b": Workload("q32b", QWEN32B, 32, (32768,) * 32, 4096, 28672,
                      description="Qwen3-32B-shaped layer; 32 decodes @32768 + 4096-token chunk on a "
                                  "28672-token cached prefix"),
+    "mchunk": Workload("mchunk", LLAMA8B, 16, (8192,) * 16, 1024, 0,
+                       more_chunks=((512, 4096), (256, 12288), (128, 2048)),
+                       description="Llama-3.1-8B-shaped layer; 16 decodes @8192 + four prefill chunks "
+                                   "(l, c) = (1024, 0), (512, 4096), (256, 12288), (128, 2048)"),
 }
 # Index order of the five measured configurations.
 WORKLOAD_ORDER = ("tiny", "l8b", "q14b", "mix", "q32b")
@@ -140,14 +147,35 @@ class Batch:
     pre_pages: np.ndarray        # [ceil((c_p + l) / ps)] page ids
     num_pages: int
     page_size: int = PAGE_SIZE
+    # further chunks (l_i, c_i, page ids) after the first chunk's rows
+    more_chunks: Tuple[Tuple[int, int, np.ndarray], ...] = ()
 
     @property
     def n_decode(self) -> int:
         return int(self.dec_ctx.shape[0])
 
     @property
+    def chunks(self):
+        """Every prefill chunk as (l_i, c_i, page ids), in stacked-row order."""
+        first = [(self.prefill_len, self.prefill_prefix, self.pre_pages)] if self.prefill_len > 0 else []
+        return first + [(int(l), int(c), p) for l, c, p in self.more_chunks]
+
+    @property
+    def prefill_rows(self) -> int:
+        return sum(l for l, _, _ in self.chunks)
+
+    @property
     def n_tokens(self) -> int:
-        return self.prefill_len + self.n_decode
+        return self.prefill_rows + self.n_decode
+
+    def chunk_table(self):
+        """(lengths, prefixes, page table [n_chunks, stride] -1 padded) of all chunks."""
+        ch = self.chunks
+        stride = max([len(p) for _, _, p in ch] + [1])
+        pages = np.full((max(len(ch), 1), stride), -1, np.int32)
+        for i, (_, _, p) in enumerate(ch):
+            pages[i, :len(p)] = p
+        return (np.array([l for l, _, _ in ch], np.int32), np.array([c for _, c, _ in ch], np.int32), pages)
 
     @property
     def dec_stride(self) -> int:
@@ -170,7 +198,8 @@ def make_batch(w: Workload, seed: int = 0) -> Batch:
     l = int(w.prefill_len)
     dec_need = (dec + 1 + ps - 1) // ps                      # pages incl. the new token
     pre_need = (cp + l + ps - 1) // ps if l > 0 else 0
-    needed = int(dec_need.sum()) + pre_need
+    more_need = [(ml + mc + ps - 1) // ps for ml, mc in w.more_chunks]
+    needed = int(dec_need.sum()) + pre_need + sum(more_need)
     num_pages = int(math.ceil(needed * w.pool_slack))
     perm = torch.randperm(num_pages, generator=_gen(seed, "pages")).numpy().astype(np.int64)
     stride = int(dec_need.max()) if len(dec) else 1
@@ -181,8 +210,12 @@ def make_batch(w: Workload, seed: int = 0) -> Batch:
     for j, n in enumerate(dec_need):
         dec_pages[j, :n] = perm[at:at + n]
         at += n
+    more = []
+    for (ml, mc), n in zip(w.more_chunks, more_need):
+        more.append((int(ml), int(mc), perm[at:at + n].astype(np.int32)))
+        at += n
     return Batch(w, dec.astype(np.int32), l, cp, dec_pages.astype(np.int32),
-                 pre_pages.astype(np.int32), num_pages)
+                 pre_pages.astype(np.int32), num_pages, more_chunks=tuple(more))
 
 
 def _randn_bf16(shape, g, std=1.0, device="cpu", chunk=1 << 26) -> torch.Tensor:
@@ -234,7 +267,7 @@ def make_weights(w: Workload, seed: int = 0, device="cpu", unit_gains: bool = Fa
 def make_pools(w: Workload, batch: Batch, seed: int = 0, device="cpu") -> Tuple[torch.Tensor, torch.Tensor]:
     """K and V pools [num_pages, Hkv, ps, d] bf16.
 
-    Cached positions (0..c_j-1 of each decode, 0..c_p-1 of the prefill
+    Cached positions (0..c_j-1 of each decode, 0..c_i-1 of each chunk's
     request) hold N(0, 1) values; every other slot holds the NaN sentinel.
     Values are drawn request by request, position-major, so a request's
     cached KV does not depend on the page permutation.
@@ -249,6 +282,7 @@ def make_pools(w: Workload, batch: Batch, seed: int = 0, device="cpu") -> Tuple[
         g = _gen(seed, tag, device)
         reqs = [(batch.pre_pages, batch.prefill_prefix)] if batch.prefill_len > 0 else []
         reqs += [(batch.dec_pages[j], int(batch.dec_ctx[j])) for j in range(batch.n_decode)]
+        reqs += [(p, c) for _, c, p in batch.more_chunks]   # after the decodes: earlier draws unchanged
         for pages, n in reqs:
             if n == 0:
                 continue
