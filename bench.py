@@ -164,8 +164,7 @@ def work_of(w, b):
     weights = {"qkv": 2.0 * s.qkv_dim * H, "oproj": 2.0 * H * Hq * d, "gateup": 4.0 * F * H, "down": 2.0 * H * F}
     keys = sum(int(c) + 1 for c in b.dec_ctx)
     dec_bytes = keys * Hkv * d * 2 * 2 + b.n_decode * Hq * d * 2 * 2
-    l, cp = b.prefill_len, b.prefill_prefix
-    pairs = l * cp + l * (l + 1) // 2
+    pairs = sum(l * cp + l * (l + 1) // 2 for l, cp, _ in b.chunks)
     pre_flops = 4.0 * d * Hq * pairs
     return {"gemm_flops": gemm, "weight_bytes": weights, "decode_bytes": float(dec_bytes),
             "decode_keys": keys, "prefill_flops": pre_flops, "prefill_pairs": pairs}
@@ -190,18 +189,21 @@ def oracle_sample(w, b, x, weights, kp, vp, rows):
 
 
 def reference_rows(b, frac=1.0):
-    """Bounded sample for the CPU oracle: the first 64 chunk rows + all decodes,
-    or the leading fraction `frac` of each (at least 8 chunk rows, 2 decodes)."""
-    l, nd = b.prefill_len, b.n_decode
+    """Bounded sample for the CPU oracle: the first 64 rows of the first chunk
+    + all decodes, or the leading fraction `frac` of each (at least 8 chunk
+    rows, 2 decodes)."""
+    l = b.chunks[0][0] if b.chunks else 0
+    P, nd = b.prefill_rows, b.n_decode
     nc = min(l, max(min(8, l), int(round(64 * frac))))
     ndec = min(nd, max(min(2, nd), int(round(nd * frac))))
-    return list(range(nc)) + list(range(l, l + ndec))
+    return list(range(nc)) + list(range(P, P + ndec))
 
 
 def workload_config(w, b, world):
     """The `config` object both arms report."""
     return {"workload": f"{w.name}: {w.description}", "tokens_per_step": b.n_tokens, "n_decode": b.n_decode,
-            "prefill_len": b.prefill_len, "prefill_prefix": b.prefill_prefix,
+            "prefill_len": b.prefill_rows, "prefill_prefix": b.prefill_prefix,
+            "chunks": [[int(l), int(c)] for l, c, _ in b.chunks],
             "decode_keys": int(sum(int(c) + 1 for c in b.dec_ctx)), "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2 (weights + KV > 129 MB), no flush"}
 
@@ -235,8 +237,13 @@ def run_cf(args, rank, world, local, pg):
     eng.cf_set_graphs(args.graphs)   # piecewise CUDA graphs of the linear segments
     dec_ctx = torch.as_tensor(b.dec_ctx, device=dev)
     dec_pages = torch.as_tensor(b.dec_pages, device=dev)
-    pre_pages = torch.as_tensor(b.pre_pages if len(b.pre_pages) else np.zeros(1, np.int32), device=dev)
-    batch = cf.batch_of(b.n_decode, dec_ctx, dec_pages, b.prefill_len, b.prefill_prefix, pre_pages)
+    if len(b.chunks) > 1:   # several prefill chunks: the chunk-list form of the batch
+        lens, prefixes, table = b.chunk_table()
+        pre_pages = torch.as_tensor(table, device=dev)
+        batch = cf.batch_of(b.n_decode, dec_ctx, dec_pages, 0, 0, None, chunks=(lens, prefixes, pre_pages))
+    else:
+        pre_pages = torch.as_tensor(b.pre_pages if len(b.pre_pages) else np.zeros(1, np.int32), device=dev)
+        batch = cf.batch_of(b.n_decode, dec_ctx, dec_pages, b.prefill_len, b.prefill_prefix, pre_pages)
     pool = cf.pool_of(kp, vp)
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -251,7 +258,7 @@ def run_cf(args, rank, world, local, pg):
     if st != 0:
         raise RuntimeError(msg)
     calib = None
-    if args.decode_sms == 0 and b.n_decode > 0 and b.prefill_len > 0:
+    if args.decode_sms == 0 and b.n_decode > 0 and b.prefill_rows > 0:
         # ConfluxServe §6.1: decode gets the fewest SMs that keep 90% of its solo bandwidth
         chosen = eng.cf_calibrate_decode_sms(batch, pool, 0.9)
         calib = {"rule": "min SMs reaching 90% of standalone decode bandwidth", "chosen": chosen,
@@ -383,8 +390,8 @@ def run_cf(args, rank, world, local, pg):
             reps += 1
         line["cpu_baseline"] = {"value": len(rows) * reps / secs, "unit": "tokens/s", "cores": blas_threads(),
                                 "kind": "oracle", "host_cores": os.cpu_count(),
-                                "sample": f"fp64 oracle layer step on {len(rows)} of {T} rows (first 64 chunk rows "
-                                          f"+ all decodes), {reps} repetitions, {secs:.1f} s"}
+                                "sample": f"fp64 oracle layer step on {len(rows)} of {T} rows (first 64 rows of the "
+                                          f"first chunk + all decodes), {reps} repetitions, {secs:.1f} s"}
     if args.sweep_decode_sms:
         line["decode_sms_sweep"] = sweep_decode_sms(eng, step, args, cf)
     eng.close()

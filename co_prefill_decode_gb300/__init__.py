@@ -30,7 +30,7 @@ EXPORTS = (
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
     "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
     "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate", "cf_waterfill_dispatch",
-    "cf_waterfill_assign",
+    "cf_waterfill_assign", "cf_prefill_attn_varlen",
 )
 
 
@@ -59,7 +59,9 @@ class cf_kv_pool(ctypes.Structure):
 class cf_batch(ctypes.Structure):
     _fields_ = [("n_decode", ctypes.c_int), ("dec_ctx", ctypes.c_void_p), ("dec_pages", ctypes.c_void_p),
                 ("dec_stride", ctypes.c_int), ("prefill_len", ctypes.c_int), ("prefill_prefix", ctypes.c_int),
-                ("pre_pages", ctypes.c_void_p)]
+                ("pre_pages", ctypes.c_void_p), ("n_chunks", ctypes.c_int),
+                ("chunk_len", ctypes.POINTER(ctypes.c_int)), ("chunk_prefix", ctypes.POINTER(ctypes.c_int)),
+                ("chunk_pages", ctypes.c_void_p), ("chunk_stride", ctypes.c_int)]
 
 
 class cf_latency_model(ctypes.Structure):
@@ -106,6 +108,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_layer_step": (I, [P, ctypes.POINTER(cf_batch), P, P, ctypes.POINTER(cf_kv_pool), P]),
         "cf_decode_attn": (I, [P, P, L, ctypes.POINTER(cf_kv_pool), I, P, P, I, P, L, I, P]),
         "cf_prefill_attn": (I, [P, P, ctypes.POINTER(cf_kv_pool), I, I, P, P, I, P]),
+        "cf_prefill_attn_varlen": (I, [P, P, ctypes.POINTER(cf_kv_pool), I, ctypes.POINTER(I), ctypes.POINTER(I),
+                                       P, I, P, I, P]),
         "cf_gemm": (I, [P, P, I, P, I, P, I, I, I, I, I, P, P]),
         "cf_kv_append": (I, [P, P, P, I, P, ctypes.POINTER(cf_kv_pool), I, I, I, P]),
         "cf_get_error": (I, [P, ctypes.c_char_p, I]),
@@ -234,6 +238,17 @@ class Engine:
             self.handle, _ptr(q), ctypes.byref(pool), l, prefix, _ptr(pages), _ptr(out), num_sms,
             _stream(stream)))
 
+    def cf_prefill_attn_varlen(self, q, pool: cf_kv_pool, chunk_len, chunk_prefix, chunk_pages, out,
+                               num_sms: int = 0, stream=None):
+        """chunk_len / chunk_prefix: host int sequences; chunk_pages: device
+        int32 [n_chunks, stride]."""
+        n = len(chunk_len)
+        ln = (ctypes.c_int * max(n, 1))(*[int(v) for v in chunk_len])
+        pf = (ctypes.c_int * max(n, 1))(*[int(v) for v in chunk_prefix])
+        _check(self.lib, self.handle, self.lib.cf_prefill_attn_varlen(
+            self.handle, _ptr(q), ctypes.byref(pool), n, ln, pf, _ptr(chunk_pages), int(chunk_pages.shape[1]),
+            _ptr(out), num_sms, _stream(stream)))
+
     def cf_gemm(self, A, B, C, epilogue: int = CF_EPI_NONE, aux=None, stream=None):
         M, K = A.shape
         N = C.shape[1]
@@ -351,10 +366,25 @@ def pool_of(k_pool: torch.Tensor, v_pool: torch.Tensor) -> cf_kv_pool:
     return cf_kv_pool(_ptr(k_pool), _ptr(v_pool), int(k_pool.shape[0]))
 
 
-def batch_of(n_decode: int, dec_ctx, dec_pages, prefill_len: int, prefill_prefix: int, pre_pages) -> cf_batch:
+def batch_of(n_decode: int, dec_ctx, dec_pages, prefill_len: int, prefill_prefix: int, pre_pages,
+             chunks=None) -> cf_batch:
+    """The batch of one step.  One prefill chunk: prefill_len / prefill_prefix /
+    pre_pages.  Several: chunks = (lengths, prefixes, device int32 page table
+    [n_chunks, stride]) with prefill_len 0."""
     stride = int(dec_pages.shape[1]) if dec_pages is not None and dec_pages.dim() == 2 else 1
-    return cf_batch(n_decode, _ptr(dec_ctx) if n_decode else None, _ptr(dec_pages) if n_decode else None, stride,
-                    prefill_len, prefill_prefix, _ptr(pre_pages) if prefill_len else None)
+    b = cf_batch(n_decode, _ptr(dec_ctx) if n_decode else None, _ptr(dec_pages) if n_decode else None, stride,
+                 prefill_len, prefill_prefix, _ptr(pre_pages) if prefill_len else None)
+    if chunks is not None:
+        lens, prefixes, pages = chunks
+        n = len(lens)
+        b._chunk_arrays = ((ctypes.c_int * max(n, 1))(*[int(v) for v in lens]),
+                           (ctypes.c_int * max(n, 1))(*[int(v) for v in prefixes]), pages)
+        b.n_chunks = n
+        b.chunk_len = b._chunk_arrays[0]
+        b.chunk_prefix = b._chunk_arrays[1]
+        b.chunk_pages = _ptr(pages)
+        b.chunk_stride = int(pages.shape[1])
+    return b
 
 
 # ---------------------------------------------------------------------------

@@ -147,13 +147,13 @@ struct cf_engine {
   // piecewise CUDA graphs of the shared linear segments (ConfluxServe §6.1, Fig. 10)
   int use_graphs = 0;
   cudaStream_t cstream = nullptr;    // capture stream
-  int* bdev = nullptr;               // device batch descriptor: chunk length, prefix
+  ChunkRows* bdev = nullptr;         // device copy of the step's chunk table (graph replay)
   struct Graphs {
     long long T;
     const void *x_in, *x_out, *pk, *pv;
     int num_pages;
     const int *dec_ctx, *dec_pages, *pre_pages;
-    int dec_stride, split_mode;
+    int dec_stride, pre_stride, split_mode;
     cudaGraphExec_t a, b;            // RMSNorm + QKV; O-proj + RMSNorm + gate/up + down
   };
   std::vector<Graphs> graphs;
@@ -225,24 +225,102 @@ cf_status check_pool(cf_engine* e, const cf_kv_pool* pool) {
   return CF_OK;
 }
 
-cf_status check_batch(cf_engine* e, const cf_batch* bt) {
+// The prefill chunks of a batch: the chunk list when n_chunks > 0, else the
+// single chunk of prefill_len / prefill_prefix / pre_pages (or none).
+struct StepChunks {
+  int n = 0;
+  int len[kMaxChunks], prefix[kMaxChunks];
+  const int* pages = nullptr;   // chunk i's table at pages + i * stride
+  int stride = 0;
+  int rows = 0;                 // prefill rows, sum of len
+};
+
+cf_status chunks_of(cf_engine* e, const cf_batch* bt, StepChunks* ch) {
+  ch->n = 0;
+  ch->rows = 0;
+  if (bt->n_chunks < 0) return fail(e, CF_ERR_INVALID_ARG, "negative n_chunks");
+  if (bt->n_chunks > 0) {
+    if (bt->prefill_len != 0) return fail(e, CF_ERR_INVALID_ARG, "prefill_len must be 0 when n_chunks > 0");
+    if (bt->n_chunks > kMaxChunks) return fail(e, CF_ERR_UNSUPPORTED, "more than 32 prefill chunks");
+    if (!bt->chunk_len || !bt->chunk_prefix || !bt->chunk_pages || bt->chunk_stride <= 0)
+      return fail(e, CF_ERR_INVALID_ARG, "prefill chunks without lengths, prefixes or page tables");
+    long long rows = 0;
+    for (int i = 0; i < bt->n_chunks; ++i) {
+      const int l = bt->chunk_len[i], c = bt->chunk_prefix[i];
+      if (l <= 0 || c < 0) return fail(e, CF_ERR_INVALID_ARG, "chunk length < 1 or negative prefix");
+      if (((long long)c + l + e->cfg.page_size - 1) / e->cfg.page_size > bt->chunk_stride)
+        return fail(e, CF_ERR_INVALID_ARG, "chunk needs more pages than chunk_stride");
+      ch->len[i] = l;
+      ch->prefix[i] = c;
+      rows += l;
+      if (rows > e->cfg.max_tokens) return fail(e, CF_ERR_INVALID_ARG, "batch exceeds engine limits");
+    }
+    ch->n = bt->n_chunks;
+    ch->rows = (int)rows;
+    ch->pages = bt->chunk_pages;
+    ch->stride = bt->chunk_stride;
+    return CF_OK;
+  }
+  if (bt->prefill_len < 0 || bt->prefill_prefix < 0) return fail(e, CF_ERR_INVALID_ARG, "negative batch sizes");
+  if (bt->prefill_len > 0) {
+    if (!bt->pre_pages) return fail(e, CF_ERR_INVALID_ARG, "prefill chunk without a page table");
+    ch->n = 1;
+    ch->len[0] = bt->prefill_len;
+    ch->prefix[0] = bt->prefill_prefix;
+    ch->rows = bt->prefill_len;
+    ch->pages = bt->pre_pages;
+  }
+  return CF_OK;
+}
+
+cf_status check_batch(cf_engine* e, const cf_batch* bt, StepChunks* ch) {
   const cf_config& c = e->cfg;
-  const int l = bt->prefill_len, nd = bt->n_decode;
-  if (l < 0 || nd < 0 || bt->prefill_prefix < 0) return fail(e, CF_ERR_INVALID_ARG, "negative batch sizes");
-  if ((long long)l + nd > c.max_tokens || nd > c.max_decode)
+  cf_status st = chunks_of(e, bt, ch);
+  if (st != CF_OK) return st;
+  const int nd = bt->n_decode;
+  if (nd < 0) return fail(e, CF_ERR_INVALID_ARG, "negative batch sizes");
+  if ((long long)ch->rows + nd > c.max_tokens || nd > c.max_decode)
     return fail(e, CF_ERR_INVALID_ARG, "batch exceeds engine limits");
   if (nd > 0 && (!bt->dec_ctx || !bt->dec_pages || bt->dec_stride <= 0))
     return fail(e, CF_ERR_INVALID_ARG, "decode batch without context/page arrays");
-  if (l > 0 && !bt->pre_pages) return fail(e, CF_ERR_INVALID_ARG, "prefill chunk without a page table");
   return CF_OK;
+}
+
+ChunkRows chunk_rows(const StepChunks& ch) {
+  ChunkRows cr{};
+  cr.n = ch.n;
+  int r = 0;
+  for (int i = 0; i < ch.n; ++i) {
+    cr.row0[i] = r;
+    cr.prefix[i] = ch.prefix[i];
+    r += ch.len[i];
+  }
+  cr.row0[ch.n] = r;
+  return cr;
+}
+
+// The chunk slots of a prefill launch: chunk i's rows of q and of out start
+// at the sum of the earlier chunks' lengths.
+void prefill_chunks_args(cf_engine* e, const StepChunks& ch, PrefillArgs& pf) {
+  int row0[kMaxChunks], off[kMaxChunks];
+  int r = 0;
+  for (int i = 0; i < ch.n; ++i) {
+    row0[i] = r;
+    off[i] = i * ch.stride;
+    r += ch.len[i];
+  }
+  pf.pages = ch.pages;
+  pf.pair = e->prefill_pair ? e->prefill_pair - 1 : prefill_pairing(ch.len, ch.n, pf.Hq, e->sms);
+  prefill_set_chunks(pf, ch.n, ch.len, ch.prefix, row0, off);
 }
 
 // RoPE table + slots (and optionally the RMSNorm of x), then the fused QKV
 // GEMM whose epilogue writes q and appends k, v.
-cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const void* x, const CUtensorMap& tm_xn, void* q_out,
-                    const cf_kv_pool* pool, cudaStream_t s, cudaEvent_t ev_mid, const int* bdev = nullptr) {
+cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const StepChunks& ch, const void* x, const CUtensorMap& tm_xn,
+                    void* q_out, const cf_kv_pool* pool, cudaStream_t s, cudaEvent_t ev_mid,
+                    const ChunkRows* bdev = nullptr) {
   const cf_config& c = e->cfg;
-  const int T = bt->prefill_len + bt->n_decode;
+  const int T = ch.rows + bt->n_decode;
   PrepArgs pa{};
   pa.x = x;
   pa.in_f32 = 0;
@@ -255,13 +333,13 @@ cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const void* x, const CUten
   pa.inv_freq = e->inv_freq;
   pa.half_dim = c.head_dim / 2;
   pa.slot = e->slot;
-  pa.l = bt->prefill_len;
-  pa.prefix = bt->prefill_prefix;
+  pa.cr = chunk_rows(ch);
   pa.n_decode = bt->n_decode;
   pa.dec_ctx = bt->dec_ctx;
   pa.dec_pages = bt->dec_pages;
   pa.dec_stride = bt->dec_stride;
-  pa.pre_pages = bt->pre_pages;
+  pa.pre_pages = ch.pages;
+  pa.pre_stride = ch.stride;
   pa.num_pages = pool->num_pages;
   pa.page_size = c.page_size;
   pa.err = e->err;
@@ -380,7 +458,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   const size_t o_cs = take(T * (d / 2) * 8), o_slot = take(T * 4), o_inv = take(d / 2 * 8);
   const size_t o_po = take((size_t)e->max_items * G * d * 4), o_pml = take((size_t)e->max_items * G * 2 * 4);
   const size_t o_plan = take((size_t)(c.max_decode + 4) * 4), o_cnt = take(4), o_err = take(4);
-  const size_t o_dcnt = take(4), o_bdev = take(16);
+  const size_t o_dcnt = take(4), o_bdev = take(sizeof(ChunkRows));
   const size_t o_skw = take(gemm_sk_ws_bytes(e->sms)), o_skf = take(gemm_sk_flag_bytes(e->sms));
   e->ws_bytes = off;
   if (cudaMalloc(&e->ws, off) != cudaSuccess) {
@@ -404,7 +482,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   e->counter = reinterpret_cast<unsigned*>(b + o_cnt);
   e->err = reinterpret_cast<int*>(b + o_err);
   e->dec_counter = reinterpret_cast<int*>(b + o_dcnt);
-  e->bdev = reinterpret_cast<int*>(b + o_bdev);
+  e->bdev = reinterpret_cast<ChunkRows*>(b + o_bdev);
   e->sk_ws = reinterpret_cast<float*>(b + o_skw);
   e->sk_flags = reinterpret_cast<int*>(b + o_skf);
   bool ok = cudaMemset(e->ws, 0, off) == cudaSuccess;
@@ -527,13 +605,14 @@ cf_status ffn_stage(cf_engine* e, long long T, const void* x_in, void* x_out, cu
 }
 
 // The graphs of one (T, buffers) key, captured on first use.
-cf_engine::Graphs* graphs_for(cf_engine* e, const cf_batch* bt, long long T, const void* x_in, void* x_out,
-                              const cf_kv_pool* pool, cf_status* st) {
+cf_engine::Graphs* graphs_for(cf_engine* e, const cf_batch* bt, const StepChunks& ch, long long T, const void* x_in,
+                              void* x_out, const cf_kv_pool* pool, cf_status* st) {
   *st = CF_OK;
   for (auto& g : e->graphs)
     if (g.T == T && g.x_in == x_in && g.x_out == x_out && g.pk == pool->k && g.pv == pool->v &&
         g.num_pages == pool->num_pages && g.dec_ctx == bt->dec_ctx && g.dec_pages == bt->dec_pages &&
-        g.pre_pages == bt->pre_pages && g.dec_stride == bt->dec_stride && g.split_mode == e->split_mode)
+        g.pre_pages == ch.pages && g.dec_stride == bt->dec_stride && g.pre_stride == ch.stride &&
+        g.split_mode == e->split_mode)
       return &g;
   if (e->graphs.size() >= 16) {   // keep the cache small: drop the oldest
     cudaGraphExecDestroy(e->graphs.front().a);
@@ -541,12 +620,12 @@ cf_engine::Graphs* graphs_for(cf_engine* e, const cf_batch* bt, long long T, con
     e->graphs.erase(e->graphs.begin());
   }
   cf_engine::Graphs g{T, x_in, x_out, pool->k, pool->v, pool->num_pages, bt->dec_ctx, bt->dec_pages,
-                      bt->pre_pages, bt->dec_stride, e->split_mode, nullptr, nullptr};
+                      ch.pages, bt->dec_stride, ch.stride, e->split_mode, nullptr, nullptr};
   const long long launches = e->launches;   // captured launches do not run now
   cudaGraph_t ga = nullptr, gb = nullptr;
   cudaError_t r = cudaStreamBeginCapture(e->cstream, cudaStreamCaptureModeThreadLocal);
   if (r == cudaSuccess) {
-    *st = qkv_stage(e, bt, x_in, e->tm.xn, e->q, pool, e->cstream, nullptr, e->bdev);
+    *st = qkv_stage(e, bt, ch, x_in, e->tm.xn, e->q, pool, e->cstream, nullptr, e->bdev);
     r = cudaStreamEndCapture(e->cstream, &ga);
   }
   if (r == cudaSuccess && *st == CF_OK) {
@@ -577,9 +656,10 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
                         void* stream) {
   if (!e || !bt || !x_in || !x_out) return fail(e, CF_ERR_INVALID_ARG, "null argument");
   const cf_config& c = e->cfg;
-  cf_status st = check_batch(e, bt);
+  StepChunks ch;
+  cf_status st = check_batch(e, bt, &ch);
   if (st != CF_OK) return st;
-  const int l = bt->prefill_len, nd = bt->n_decode;
+  const int l = ch.rows, nd = bt->n_decode;   // l: prefill rows of all chunks
   const long long T = (long long)l + nd;
   if (T == 0) return CF_OK;
   if (!aligned16(x_in) || !aligned16(x_out)) return fail(e, CF_ERR_INVALID_ARG, "x not 16-byte aligned");
@@ -608,20 +688,20 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
 
   // a1 + a2: RMSNorm (+ RoPE table, slots), fused QKV GEMM with append.
   // With graphs on, this segment and a6 - a9 replay captured graphs; the
-  // batch's chunk length and prefix reach the captured RMSNorm kernel through
-  // a small device descriptor written just before.
+  // batch's chunk lengths and prefixes reach the captured RMSNorm kernel
+  // through a small device copy of the chunk table written just before.
   cf_engine::Graphs* ge = nullptr;
   if (e->use_graphs && !ev) {
-    ge = graphs_for(e, bt, T, x_in, x_out, pool, &st);
+    ge = graphs_for(e, bt, ch, T, x_in, x_out, pool, &st);
     if (st != CF_OK) return st;
   }
   if (ge) {
-    const int hb[2] = {l, bt->prefill_prefix};
-    CF_CUDA(e, cudaMemcpyAsync(e->bdev, hb, sizeof(hb), cudaMemcpyHostToDevice, s));
+    const ChunkRows hb = chunk_rows(ch);
+    CF_CUDA(e, cudaMemcpyAsync(e->bdev, &hb, sizeof(hb), cudaMemcpyHostToDevice, s));
     CF_CUDA(e, cudaGraphLaunch(ge->a, s));
     e->launches += 2;
   } else {
-    st = qkv_stage(e, bt, x_in, e->tm.xn, e->q, pool, s, ev ? ev[EV_PREP] : nullptr);
+    st = qkv_stage(e, bt, ch, x_in, e->tm.xn, e->q, pool, s, ev ? ev[EV_PREP] : nullptr);
     if (st != CF_OK) return st;
   }
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_QKV], s));
@@ -665,19 +745,16 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     da.err = e->err;
   }
   if (l > 0) {
-    pf.l = l;
-    pf.prefix = bt->prefill_prefix;
     pf.Hq = Hq;
     pf.Hkv = c.n_kv_heads;
     pf.head_dim = d;
     pf.page_size = c.page_size;
     pf.num_pages = pool->num_pages;
-    pf.pages = bt->pre_pages;
     pf.out = e->attn;
     pf.out_stride = (long long)Hq * d;
     pf.scale_log2 = scale_log2;
-    pf.pair = e->prefill_pair ? e->prefill_pair - 1 : prefill_pairing(pf.l, pf.Hq, e->sms);
-  pf.counter = e->counter;   // zeroed by this step's prep kernel
+    prefill_chunks_args(e, ch, pf);
+    pf.counter = e->counter;   // zeroed by this step's prep kernel
     pf.base = 0;
     pf.err = e->err;
     pf.wait_ns = kWaitNs;
@@ -742,9 +819,10 @@ cf_status cf_rmsnorm(cf_engine* e, const void* x, int x_is_f32, const void* gain
 cf_status cf_qkv(cf_engine* e, const cf_batch* bt, const void* xn, const cf_kv_pool* pool, void* q_out,
                  void* stream) {
   if (!e || !bt || !xn || !q_out) return fail(e, CF_ERR_INVALID_ARG, "null argument");
-  cf_status st = check_batch(e, bt);
+  StepChunks ch;
+  cf_status st = check_batch(e, bt, &ch);
   if (st != CF_OK) return st;
-  const int T = bt->prefill_len + bt->n_decode;
+  const int T = ch.rows + bt->n_decode;
   if (T == 0) return CF_OK;
   if (!aligned16(xn) || !aligned16(q_out)) return fail(e, CF_ERR_INVALID_ARG, "not 16-byte aligned");
   st = check_pool(e, pool);
@@ -752,7 +830,7 @@ cf_status cf_qkv(cf_engine* e, const cf_batch* bt, const void* xn, const cf_kv_p
   CUtensorMap tm;
   if (!make_tmap_2d(&tm, xn, T, e->cfg.hidden, e->cfg.hidden, 128, 64))
     return fail(e, CF_ERR_CUDA, "cuTensorMapEncodeTiled failed for xn");
-  return qkv_stage(e, bt, nullptr, tm, q_out, pool, static_cast<cudaStream_t>(stream), nullptr);
+  return qkv_stage(e, bt, ch, nullptr, tm, q_out, pool, static_cast<cudaStream_t>(stream), nullptr);
 }
 
 cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride, const cf_kv_pool* pool, int n,
@@ -804,12 +882,12 @@ cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride, co
   return CF_OK;
 }
 
-cf_status cf_prefill_attn(cf_engine* e, const void* q, const cf_kv_pool* pool, int l, int prefix, const int* pages,
-                          void* out, int num_sms, void* stream) {
-  if (!e) return CF_ERR_INVALID_ARG;
-  if (l < 0 || prefix < 0) return fail(e, CF_ERR_INVALID_ARG, "negative sizes");
-  if (l == 0) return CF_OK;
-  if (!q || !pages || !out) return fail(e, CF_ERR_INVALID_ARG, "null argument");
+namespace {
+
+cf_status prefill_attn_impl(cf_engine* e, const void* q, const cf_kv_pool* pool, const StepChunks& ch, void* out,
+                            int num_sms, cudaStream_t s) {
+  if (ch.rows == 0) return CF_OK;
+  if (!q || !out) return fail(e, CF_ERR_INVALID_ARG, "null argument");
   if (!aligned16(q) || !aligned16(out)) return fail(e, CF_ERR_INVALID_ARG, "q/out not 16-byte aligned");
   const cf_config& c = e->cfg;
   cf_status st = check_pool(e, pool);
@@ -817,31 +895,64 @@ cf_status cf_prefill_attn(cf_engine* e, const void* q, const cf_kv_pool* pool, i
   st = pool_maps(e, pool);
   if (st != CF_OK) return st;
   CUtensorMap tq;
-  if (!make_tmap_3d(&tq, q, c.head_dim, c.n_q_heads, l, c.head_dim, (uint64_t)c.n_q_heads * c.head_dim, 64, 1, 128))
+  if (!make_tmap_3d(&tq, q, c.head_dim, c.n_q_heads, ch.rows, c.head_dim, (uint64_t)c.n_q_heads * c.head_dim, 64,
+                    1, 128))
     return fail(e, CF_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
   int ctas = num_sms > 0 ? num_sms : e->sms;
   if (ctas > e->sms) ctas = e->sms;
   PrefillArgs pf{};
-  pf.l = l;
-  pf.prefix = prefix;
   pf.Hq = c.n_q_heads;
   pf.Hkv = c.n_kv_heads;
   pf.head_dim = c.head_dim;
   pf.page_size = c.page_size;
   pf.num_pages = pool->num_pages;
-  pf.pages = pages;
   pf.out = static_cast<__nv_bfloat16*>(out);
   pf.out_stride = (long long)c.n_q_heads * c.head_dim;
   pf.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
-  pf.pair = e->prefill_pair ? e->prefill_pair - 1 : prefill_pairing(pf.l, pf.Hq, e->sms);
+  prefill_chunks_args(e, ch, pf);
   pf.counter = e->counter;
   pf.base = 0;
-  CF_CUDA(e, cudaMemsetAsync(e->counter, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream)));
+  CF_CUDA(e, cudaMemsetAsync(e->counter, 0, sizeof(unsigned), s));
   pf.err = e->err;
   pf.wait_ns = kWaitNs;
-  CF_CUDA(e, launch_prefill(tq, e->pm.tk, e->pm.tv, pf, ctas, static_cast<cudaStream_t>(stream)));
+  CF_CUDA(e, launch_prefill(tq, e->pm.tk, e->pm.tv, pf, ctas, s));
   e->launches++;
   return CF_OK;
+}
+
+}  // namespace
+
+cf_status cf_prefill_attn(cf_engine* e, const void* q, const cf_kv_pool* pool, int l, int prefix, const int* pages,
+                          void* out, int num_sms, void* stream) {
+  if (!e) return CF_ERR_INVALID_ARG;
+  if (l < 0 || prefix < 0) return fail(e, CF_ERR_INVALID_ARG, "negative sizes");
+  if (l == 0) return CF_OK;
+  if (!pages) return fail(e, CF_ERR_INVALID_ARG, "null argument");
+  StepChunks ch;
+  ch.n = 1;
+  ch.len[0] = l;
+  ch.prefix[0] = prefix;
+  ch.rows = l;
+  ch.pages = pages;
+  return prefill_attn_impl(e, q, pool, ch, out, num_sms, static_cast<cudaStream_t>(stream));
+}
+
+cf_status cf_prefill_attn_varlen(cf_engine* e, const void* q, const cf_kv_pool* pool, int n_chunks,
+                                 const int* chunk_len, const int* chunk_prefix, const int* chunk_pages,
+                                 int chunk_stride, void* out, int num_sms, void* stream) {
+  if (!e) return CF_ERR_INVALID_ARG;
+  if (n_chunks < 0) return fail(e, CF_ERR_INVALID_ARG, "negative n_chunks");
+  if (n_chunks == 0) return CF_OK;
+  cf_batch b{};
+  b.n_chunks = n_chunks;
+  b.chunk_len = chunk_len;
+  b.chunk_prefix = chunk_prefix;
+  b.chunk_pages = chunk_pages;
+  b.chunk_stride = chunk_stride;
+  StepChunks ch;
+  const cf_status st = chunks_of(e, &b, &ch);
+  if (st != CF_OK) return st;
+  return prefill_attn_impl(e, q, pool, ch, out, num_sms, static_cast<cudaStream_t>(stream));
 }
 
 cf_status cf_gemm(cf_engine* e, const void* A, int lda, const void* B, int ldb, void* C, int ldc, int M, int N, int K,
@@ -1011,7 +1122,8 @@ cf_status cf_set_decode_sms(cf_engine* e, int n) {
 cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* bt, const cf_kv_pool* pool, float frac,
                                   void* stream, int* chosen) {
   if (!e || !bt || !chosen || !(frac > 0.f && frac <= 1.f)) return fail(e, CF_ERR_INVALID_ARG, "bad argument");
-  cf_status st = check_batch(e, bt);
+  StepChunks ch;
+  cf_status st = check_batch(e, bt, &ch);
   if (st != CF_OK) return st;
   if (bt->n_decode == 0) return fail(e, CF_ERR_INVALID_ARG, "no decode requests to calibrate on");
   st = check_pool(e, pool);
@@ -1022,7 +1134,7 @@ cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* bt, const cf_kv_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t row = (size_t)c.n_q_heads * c.head_dim;
   DecodeArgs da{};
-  da.q = e->q + (size_t)bt->prefill_len * row;   // Q rows of the last step's decodes
+  da.q = e->q + (size_t)ch.rows * row;   // Q rows of the last step's decodes
   da.q_stride = (long long)row;
   da.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
   da.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
@@ -1032,7 +1144,7 @@ cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* bt, const cf_kv_
   da.key_offset = 1;
   da.pages = bt->dec_pages;
   da.page_stride = bt->dec_stride;
-  da.out = e->attn + (size_t)bt->prefill_len * row;
+  da.out = e->attn + (size_t)ch.rows * row;
   da.out_stride = (long long)row;
   da.Hq = c.n_q_heads;
   da.Hkv = c.n_kv_heads;

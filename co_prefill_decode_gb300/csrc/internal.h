@@ -98,6 +98,16 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB0, const C
 int gemm_block_n(int epi);   // BN used for an epilogue kind
 
 // ------------------------------------------------------------------ row kernels
+// ------------------------------------------------------------------ prefill chunks
+// The prefill chunks of one step (ConfluxServe §6.2 Eq. 6: the scheduled
+// batch P), stacked one after another before the decode rows.
+constexpr int kMaxChunks = 32;
+struct ChunkRows {
+  int n;                          // chunks
+  int row0[kMaxChunks + 1];       // first stacked row of chunk i; row0[n] = prefill rows
+  int prefix[kMaxChunks];         // c_i: chunk row r sits at position c_i + r - row0[i]
+};
+
 struct PrepArgs {
   // RMSNorm
   const void* x;                  // [T][H] bf16 (in_f32 = 0) or fp32
@@ -111,15 +121,17 @@ struct PrepArgs {
   const double* inv_freq;         // [d/2]
   int half_dim;
   int* slot;                      // [T]
-  int l, prefix, n_decode;
+  ChunkRows cr;                   // the step's chunks (read from bdev instead when bdev is set)
+  int n_decode;
   const int* dec_ctx;
   const int* dec_pages;
   int dec_stride;
-  const int* pre_pages;
+  const int* pre_pages;           // chunk i's page table at pre_pages + i * pre_stride
+  int pre_stride;
   int num_pages, page_size;
   int* err;
   unsigned* zero;                 // if set, block 0 stores 0 here (resets a work queue)
-  const int* bdev;                // if set, l and prefix are read from bdev[0], bdev[1] (graph replay)
+  const ChunkRows* bdev;          // if set, the chunks are read from device memory (graph replay)
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
@@ -170,9 +182,17 @@ cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------------ prefill attention
 struct PrefillArgs {
-  int l, prefix;                  // chunk length, cached prefix
+  // Work items are numbered chunk slot by chunk slot (slots sorted so that the
+  // chunk reaching furthest into its request comes first); slot s owns items
+  // [item_end[s-1], item_end[s]).
+  int n_chunks;
+  int item_end[kMaxChunks];
+  int row0[kMaxChunks];           // the chunk's first row of Q and of out
+  int len[kMaxChunks];            // l_i
+  int prefix[kMaxChunks];         // c_i
+  int page_off[kMaxChunks];       // its page table: pages + page_off, ceil((c_i + l_i) / ps) ids
   int Hq, Hkv, head_dim, page_size, num_pages;
-  const int* pages;               // [ceil((prefix + l) / ps)]
+  const int* pages;
   __nv_bfloat16* out;             // row i at out + i * out_stride, [Hq][d]
   long long out_stride;
   float scale_log2;
@@ -185,10 +205,16 @@ struct PrefillArgs {
   unsigned long long wait_ns;
 };
 // Pair query tiles when that still leaves at least one item per SM of the device.
-inline int prefill_pairing(int l, int Hq, int sms) {
-  const int n_qt = (l + 127) / 128;
-  return ((n_qt + 1) / 2) * Hq >= sms ? 1 : 0;
+inline int prefill_pairing(const int* len, int n, int Hq, int sms) {
+  long long groups = 0;
+  for (int i = 0; i < n; ++i) groups += ((len[i] + 127) / 128 + 1) / 2;
+  return groups * Hq >= sms ? 1 : 0;
 }
+// Fills the chunk slots and item counts of `a` (a.Hq and a.pair set) from
+// chunks given in stacked-row order: lengths, prefixes, first rows and page
+// table offsets.
+void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix, const int* row0,
+                        const int* page_off);
 
 // CTAs a launch really uses (<= items), and the items of a launch.
 int prefill_grid(const PrefillArgs& a, int num_ctas);

@@ -8,10 +8,13 @@
 // are entirely masked are never visited and only tiles that cross the
 // diagonal are masked.
 //
+// Several chunks of different requests may share a launch (ConfluxServe §6.2
+// Eq. 6, the scheduled prefill batch P): each has its own rows of Q and of
+// the output, its own prefix c_i and its own page table.
 // A work item is a pair of consecutive 128-row query tiles (A, B) of one
-// query head, and every 128-key K and V tile is loaded once for both; when
-// a chunk has too few tile pairs to give every SM one, items are single
-// tiles (A only) instead.
+// query head of one chunk, and every 128-key K and V tile is loaded once for
+// both; when the chunks have too few tile pairs to give every SM one, items
+// are single tiles (A only) instead.
 // Persistent CTAs draw items from a device-wide queue (an atomic counter
 // zeroed earlier in the step), so several grids can share one chunk's items:
 // the layer step runs one grid on the prefill SM partition and, once decode
@@ -65,27 +68,39 @@ struct PfCfg {
 };
 
 struct Item {
-  int qa, qb, head;   // query tiles A and B (qb = -1: none)
+  int qa, qb, head;   // query tiles A and B (qb = -1: none) of the chunk
+  int row0, len, prefix;
+  const int* pages;   // the chunk's page table
 };
 
-// n_groups = number of tile pairs (pair) or tiles; heaviest (last) query tiles first
-CF_DEV Item item_of(int idx, int Hq, int n_groups, int pair, int n_qt) {
+// Item idx: its chunk slot, then within the slot pairs of tiles (pair) or
+// tiles, heaviest (last) query tiles first, query head fastest.
+CF_DEV Item item_at(const PrefillArgs& a, int idx) {
+  int sl = 0;
+  while (sl + 1 < a.n_chunks && a.item_end[sl] <= idx) ++sl;
+  const int local = idx - (sl ? a.item_end[sl - 1] : 0);
   Item it;
-  const int g = n_groups - 1 - idx / Hq;
-  it.head = idx % Hq;
-  it.qa = pair ? 2 * g : g;
-  it.qb = (pair && 2 * g + 1 < n_qt) ? 2 * g + 1 : -1;
+  it.row0 = a.row0[sl];
+  it.len = a.len[sl];
+  it.prefix = a.prefix[sl];
+  it.pages = a.pages + a.page_off[sl];
+  const int n_qt = (it.len + BQ - 1) / BQ;
+  const int n_groups = a.pair ? (n_qt + 1) / 2 : n_qt;
+  const int g = n_groups - 1 - local / a.Hq;
+  it.head = local % a.Hq;
+  it.qa = a.pair ? 2 * g : g;
+  it.qb = (a.pair && 2 * g + 1 < n_qt) ? 2 * g + 1 : -1;
   return it;
 }
-CF_DEV int kv_tiles(const PrefillArgs& a, int qt) {
-  const int end = min(a.prefix + qt * BQ + BQ, a.prefix + a.l);   // exclusive key end
+CF_DEV int kv_tiles(const Item& it, int qt) {
+  const int end = min(it.prefix + qt * BQ + BQ, it.prefix + it.len);   // exclusive key end
   return (end + BKV - 1) / BKV;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
   using C = PfCfg<D>;
   constexpr int NS = C::KV_STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -150,10 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, a.err, a.wait_ns};
 
   const int G = a.Hq / a.Hkv;
-  const int n_qt = (a.l + BQ - 1) / BQ;
-  const int n_groups = a.pair ? (n_qt + 1) / 2 : n_qt;
-  const int n_items = n_groups * a.Hq;
-  const int n_pages_req = (a.prefix + a.l + a.page_size - 1) / a.page_size;
+  const int n_items = a.item_end[a.n_chunks - 1];
   const int oob_row = a.num_pages * a.Hkv * a.page_size;   // first row past the pool
 
   if (warp == 0 || warp == 2) {  // ------------------------------------ producers
@@ -182,14 +194,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ring[k & 7] = idx;
             mbar_arrive(&item_ready[k & 7]);
             if (idx >= 0) {
-              const Item it0 = item_of(idx, a.Hq, n_groups, a.pair, n_qt);
+              const Item it0 = item_at(a, idx);
               const int nq = it0.qb >= 0 ? 2 : 1;
               mbar_expect_tx(q_full, nq * C::TILE);
               for (int t = 0; t < nq; ++t)
 #pragma unroll
                 for (int hd = 0; hd < D / 64; ++hd)
                   tma_load_3d(smem + C::OFF_Q + t * C::TILE + hd * C::HALF, &tmQ, q_full, hd * 64, it0.head,
-                              (t ? it0.qb : it0.qa) * BQ);
+                              it0.row0 + (t ? it0.qb : it0.qa) * BQ);
               last_q = qc & 1;
             }
           }
@@ -201,11 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       idx = __shfl_sync(0xffffffffu, idx, 0);
       if (!ok || idx < 0) break;
-      const Item it = item_of(idx, a.Hq, n_groups, a.pair, n_qt);
+      const Item it = item_at(a, idx);
       const int kvh = it.head / G;
       ++qc;
-      const int nkv = kv_tiles(a, it.qb >= 0 ? it.qb : it.qa);   // the later tile reaches furthest
-      int pid = (lane < 8 && lane < n_pages_req) ? a.pages[lane] : -1;
+      const int nkv = kv_tiles(it, it.qb >= 0 ? it.qb : it.qa);   // the later tile reaches furthest
+      const int n_pages_req = (it.prefix + it.len + a.page_size - 1) / a.page_size;
+      int pid = (lane < 8 && lane < n_pages_req) ? it.pages[lane] : -1;
       for (int j = 0; j < nkv; ++j, ++kc) {
         const int st = kc % NS;
         const uint32_t ph = (kc / NS) & 1;
@@ -219,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // page ids of the next tile, so the next copies do not wait on them
         const int pin = (j + 1) * 8 + lane;
-        const int pid_next = (lane < 8 && j + 1 < nkv && pin < n_pages_req) ? a.pages[pin] : -1;
+        const int pid_next = (lane < 8 && j + 1 < nkv && pin < n_pages_req) ? it.pages[pin] : -1;
         const int my_page = lane / (D / 64), my_hd = lane % (D / 64);
         const int my_row = __shfl_sync(0xffffffffu, row, my_page & 7);
         uint64_t* full = is_v ? &v_full[st] : &k_full[st];
@@ -287,10 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&item_ready[k & 7], (k >> 3) & 1, wc)) { ok = false; break; }
         const int idx = ring[k & 7];
         if (idx < 0) break;
-        const Item it = item_of(idx, a.Hq, n_groups, a.pair, n_qt);
+        const Item it = item_at(a, idx);
         int nt[2];
-        nt[0] = kv_tiles(a, it.qa);
-        nt[1] = it.qb >= 0 ? kv_tiles(a, it.qb) : 0;
+        nt[0] = kv_tiles(it, it.qa);
+        nt[1] = it.qb >= 0 ? kv_tiles(it, it.qb) : 0;
         const int n = nt[0] > nt[1] ? nt[0] : nt[1];
         if (!mbar_wait(q_full, qc & 1, wc)) { ok = false; break; }
         ++qc;
@@ -358,15 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&item_ready[k & 7], (k >> 3) & 1, wc)) break;
       const int idx = ring[k & 7];
       if (idx < 0) break;
-      const Item it = item_of(idx, a.Hq, n_groups, a.pair, n_qt);
+      const Item it = item_at(a, idx);
       const int qt = x ? it.qb : it.qa;
-      const int na = kv_tiles(a, it.qa);
-      const int nx = qt >= 0 ? kv_tiles(a, qt) : 0;
-      const int n = it.qb >= 0 ? kv_tiles(a, it.qb) : na;   // key tiles of the item
-      const int qi = qt * BQ + r;
-      const int qpos = a.prefix + qi;
-      const int kend = a.prefix + a.l;          // first key that does not exist
-      const int diag = a.prefix + qt * BQ;      // smallest query position of the tile
+      const int na = kv_tiles(it, it.qa);
+      const int nx = qt >= 0 ? kv_tiles(it, qt) : 0;
+      const int n = it.qb >= 0 ? kv_tiles(it, it.qb) : na;   // key tiles of the item
+      const int qi = qt * BQ + r;               // query row within the chunk
+      const int qpos = it.prefix + qi;
+      const int kend = it.prefix + it.len;      // first key that does not exist
+      const int diag = it.prefix + qt * BQ;     // smallest query position of the tile
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nx; ++j) {
         if (!mbar_wait(&s_full[x], sc & 1, wc)) { ok = false; break; }
@@ -463,13 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++odc;
       tc_fence_after();
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      __nv_bfloat16* orow = a.out + (size_t)qi * a.out_stride + (size_t)it.head * D;
+      __nv_bfloat16* orow = a.out + (size_t)(it.row0 + qi) * a.out_stride + (size_t)it.head * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         tmem_ld32(to + c * 32, o);
         tmem_ld_wait();
-        if (qi < a.l) {
+        if (qi < it.len) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -511,9 +524,32 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
 
 }  // namespace
 
-int prefill_items(const PrefillArgs& a) {
-  const int n_qt = (a.l + BQ - 1) / BQ;
-  return (a.pair ? (n_qt + 1) / 2 : n_qt) * a.Hq;
+int prefill_items(const PrefillArgs& a) { return a.n_chunks > 0 ? a.item_end[a.n_chunks - 1] : 0; }
+
+void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix, const int* row0,
+                        const int* page_off) {
+  // slot order: the chunk whose last query tile reaches furthest (most key
+  // tiles per item) first, so the queue hands out the longest items first
+  int order[kMaxChunks];
+  for (int i = 0; i < n; ++i) order[i] = i;
+  for (int i = 1; i < n; ++i)   // stable insertion sort, descending c_i + l_i
+    for (int j = i; j > 0 && prefix[order[j]] + len[order[j]] > prefix[order[j - 1]] + len[order[j - 1]]; --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
+  a.n_chunks = n;
+  int items = 0;
+  for (int s = 0; s < n; ++s) {
+    const int i = order[s];
+    const int n_qt = (len[i] + BQ - 1) / BQ;
+    items += (a.pair ? (n_qt + 1) / 2 : n_qt) * a.Hq;
+    a.item_end[s] = items;
+    a.row0[s] = row0[i];
+    a.len[s] = len[i];
+    a.prefix[s] = prefix[i];
+    a.page_off[s] = page_off[i];
+  }
 }
 
 int prefill_grid(const PrefillArgs& a, int ctas) {
@@ -524,7 +560,7 @@ int prefill_grid(const PrefillArgs& a, int ctas) {
 
 cudaError_t launch_prefill(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const PrefillArgs& a, int num_ctas, cudaStream_t s) {
-  if (a.l <= 0) return cudaSuccess;
+  if (a.n_chunks <= 0 || prefill_items(a) <= 0) return cudaSuccess;
   if (a.head_dim == 128) return launch_t<128>(tmQ, tmK, tmV, a, num_ctas, s);
   if (a.head_dim == 64) return launch_t<64>(tmQ, tmK, tmV, a, num_ctas, s);
   return cudaErrorInvalidValue;

@@ -12,11 +12,11 @@ constexpr int kPrepThreads = 256;
 // One CTA per stacked row.  RMSNorm: xn = x / sqrt(mean(x^2) + eps) * g,
 // fp32 reduction, bf16 out.  When the RoPE table is requested, the same CTA
 // also writes the row's (cos, sin) pairs at its position and its pool slot:
-// prefill row i sits at position c_p + i of the chunk's request, decode row
-// j at position c_j of its own request (ConfluxServe §4: the chunk appends
+// row r of chunk i sits at position c_i + r of that chunk's request, decode
+// row j at position c_j of its own request (ConfluxServe §4: a chunk appends
 // its K/V, each decode extends its own cache).
 template <bool IN_F32>
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constant__ PrepArgs a) {
   const int row = blockIdx.x;
   const int H = a.H;
   __shared__ float red[kPrepThreads / 32];
@@ -81,19 +81,24 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
   }
   if (a.rope_cs == nullptr) return;
 
-  // position and pool slot of this row; a replayed graph reads the chunk
-  // length and prefix of the current batch from device memory
-  const int l = a.bdev ? a.bdev[0] : a.l;
-  const int prefix = a.bdev ? a.bdev[1] : a.prefix;
+  // position and pool slot of this row; a replayed graph reads the chunks
+  // of the current batch from device memory
+  const ChunkRows& cr = a.bdev ? *a.bdev : a.cr;
+  const int n_chunks = cr.n;
+  const int rows = cr.row0[n_chunks];
   long long pos;
   const int* table;
   int table_len;
-  if (row < l) {
-    pos = (long long)prefix + row;
-    table = a.pre_pages;
-    table_len = (prefix + l + a.page_size - 1) / a.page_size;
+  if (row < rows) {
+    int i = 0;
+    while (i + 1 < n_chunks && cr.row0[i + 1] <= row) ++i;
+    const int prefix = cr.prefix[i];
+    const int len = cr.row0[i + 1] - cr.row0[i];
+    pos = (long long)prefix + (row - cr.row0[i]);
+    table = a.pre_pages + (size_t)i * a.pre_stride;
+    table_len = (prefix + len + a.page_size - 1) / a.page_size;
   } else {
-    const int j = row - l;
+    const int j = row - rows;
     pos = a.dec_ctx[j];
     table = a.dec_pages + (size_t)j * a.dec_stride;
     table_len = a.dec_stride;

@@ -93,9 +93,13 @@ typedef struct {
     int num_pages;
 } cf_kv_pool;
 
-/* One iteration's batch: a prefill chunk and n_decode resident decodes
- * (ConfluxServe §6.2: chunk l_i with processed context c_i; decode requests
- * with context c_i).  Rows of x are [l chunk rows; n_decode decode rows]. */
+/* One iteration's batch: prefill chunks and n_decode resident decodes
+ * (ConfluxServe §6.2: the scheduled prefill batch P, chunk l_i of a request
+ * with processed context c_i; decode requests with context c_i).  Rows of x
+ * are [chunk rows; n_decode decode rows], the chunks one after another.
+ * One chunk can be given in prefill_len / prefill_prefix / pre_pages; any
+ * number up to 32 in the n_chunks arrays (then prefill_len must be 0).
+ * Fields a caller leaves zero mean "none". */
 typedef struct {
     int n_decode;
     const int* dec_ctx;    /* device int32 [n_decode]: c_j, tokens cached before
@@ -107,6 +111,14 @@ typedef struct {
     int prefill_len;       /* l, 0 = no chunk                                   */
     int prefill_prefix;    /* c_p: chunk token i sits at position c_p + i       */
     const int* pre_pages;  /* device int32 [ceil((c_p + l) / page_size)]       */
+    int n_chunks;          /* 0: the chunk above (or none); 1..32: these chunks */
+    const int* chunk_len;  /* HOST int32 [n_chunks]: l_i >= 1                   */
+    const int* chunk_prefix; /* HOST int32 [n_chunks]: c_i >= 0; row r of chunk
+                              i sits at position c_i + r of its own request     */
+    const int* chunk_pages;  /* device int32 [n_chunks][chunk_stride]: chunk i's
+                              page table, ceil((c_i + l_i) / page_size) valid
+                              entries (chunk_stride or fewer)                   */
+    int chunk_stride;
 } cf_batch;
 
 /* Piecewise CUDA graphs (ConfluxServe §6.1, Fig. 10), off by default.  When
@@ -196,6 +208,19 @@ cf_status cf_decode_attn(cf_engine* e, const void* q, long long q_row_stride,
 cf_status cf_prefill_attn(cf_engine* e, const void* q, const cf_kv_pool* pool, int l,
                           int prefix, const int* pages, void* out, int num_sms,
                           void* stream);
+
+/* Several chunks of different requests in one launch (ConfluxServe §6.2
+ * Eq. 6: the scheduled prefill batch P), each as in cf_prefill_attn: chunk
+ * i's queries are rows [r_i, r_i + l_i) of q and of out, r_i the sum of the
+ * earlier chunks' lengths, and attend to their own request's keys
+ * 0..c_i + row through chunk i's page table.  chunk_len, chunk_prefix: HOST
+ * int32 [n_chunks] (1 <= n_chunks <= 32, l_i >= 1, c_i >= 0); chunk_pages:
+ * device int32 [n_chunks][chunk_stride].  The items of all chunks share one
+ * work queue.  CF_ERR_INVALID_ARG for a bad length, prefix or stride,
+ * CF_ERR_UNSUPPORTED for more than 32 chunks. */
+cf_status cf_prefill_attn_varlen(cf_engine* e, const void* q, const cf_kv_pool* pool, int n_chunks,
+                                 const int* chunk_len, const int* chunk_prefix, const int* chunk_pages,
+                                 int chunk_stride, void* out, int num_sms, void* stream);
 
 /* RMSNorm of T rows of width H (the engine's hidden size): out = x /
  * sqrt(mean(x^2) + eps) * gain, fp32 reduction (the pre-attention and

@@ -72,8 +72,16 @@ class LayerSetup:
                                   decode_sms)
         self.eng = cf.Engine(self.cfg, self.W)
         self.pool = cf.pool_of(self.kp, self.vp)
-        self.batch = cf.batch_of(b.n_decode, self.dec_ctx, self.dec_pages, b.prefill_len, b.prefill_prefix,
-                                 self.pre_pages)
+        self.multi = len(b.chunks) > 1
+        if self.multi:   # the chunk-list form of the batch
+            lens, prefixes, table = b.chunk_table()
+            self.chunk_len, self.chunk_prefix = lens, prefixes
+            self.chunk_pages = torch.as_tensor(table, device="cuda")
+            self.batch = cf.batch_of(b.n_decode, self.dec_ctx, self.dec_pages, 0, 0, None,
+                                     chunks=(lens, prefixes, self.chunk_pages))
+        else:
+            self.batch = cf.batch_of(b.n_decode, self.dec_ctx, self.dec_pages, b.prefill_len, b.prefill_prefix,
+                                     self.pre_pages)
         self.out = torch.empty_like(self.x)
 
     def step(self):

@@ -304,6 +304,89 @@ def test_prefill_pairs_change_no_bit(cf, name, shape, l, cp):
     assert torch.equal(outs[0], outs[1])
 
 
+# several chunks of different requests in one launch (ConfluxServe §6.2
+# Eq. 6): (shape, [(l_i, c_i)]) with ragged lengths, tile edges, empty and
+# long prefixes
+VARLEN_CASES = [
+    ("tiny", wl.TINY, [(64, 128), (37, 0), (130, 300), (1, 17)]),
+    ("l8b", wl.LLAMA8B, [(300, 0), (130, 2000), (129, 700), (1, 5), (256, 4096)]),
+    ("q14b", wl.QWEN14B, [(1, 255), (128, 0), (513, 77)]),
+    ("q32b-one", wl.QWEN32B, [(256, 1000)]),
+]
+
+
+def varlen_setup(shape, chunks, seed):
+    w = wl.Workload("v", shape, 0, (), chunks[0][0], chunks[0][1], more_chunks=tuple(chunks[1:]))
+    b = wl.make_batch(w, seed)
+    kp, vp = wl.make_pools(w, b, seed, "cuda")
+    for i, (l, c, pages) in enumerate(b.chunks):   # each chunk's own K/V (appended before attention)
+        fill_positions(kp, vp, pages, c, l, 60 + 2 * i)
+    lens, prefixes, table = b.chunk_table()
+    return b, kp, vp, lens, prefixes, torch.as_tensor(table, device="cuda")
+
+
+@pytest.mark.parametrize("name,shape,chunks", VARLEN_CASES, ids=[c[0] for c in VARLEN_CASES])
+@pytest.mark.parametrize("pairing", [0, 1, 2])
+def test_prefill_varlen_matches_oracle(cf, name, shape, chunks, pairing):
+    b, kp, vp, lens, prefixes, table = varlen_setup(shape, chunks, 6)
+    Hq, d = shape.n_q_heads, shape.head_dim
+    P = int(lens.sum())
+    q = randn_bf16((P, Hq, d), 16)
+    out = torch.full((P, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    eng = engine_for(cf, shape)
+    eng.cf_set_prefill_pairing(pairing)
+    eng.cf_prefill_attn_varlen(q, cf.pool_of(kp, vp), lens, prefixes, table, out)
+    torch.cuda.synchronize()
+    assert eng.cf_get_error()[0] == 0
+    eng.cf_set_prefill_pairing(0)
+    r0 = 0
+    for l, c, pages in b.chunks:
+        ref = oracle.prefill_attention(f64(q[r0:r0 + l]), kp, vp, c, pages, 16)
+        assert_close(out[r0:r0 + l], ref, f"varlen {name} chunk ({l}, {c})")
+        r0 += l
+
+
+@pytest.mark.parametrize("name,shape,chunks", VARLEN_CASES, ids=[c[0] for c in VARLEN_CASES])
+def test_prefill_varlen_rows_equal_each_chunk_alone(cf, name, shape, chunks):
+    """A chunk's rows do not depend on the other chunks sharing the launch:
+    bit-identical to the chunk launched alone (same tiles, same key order)."""
+    b, kp, vp, lens, prefixes, table = varlen_setup(shape, chunks, 7)
+    Hq, d = shape.n_q_heads, shape.head_dim
+    P = int(lens.sum())
+    q = randn_bf16((P, Hq, d), 17)
+    eng = engine_for(cf, shape)
+    for mode in (1, 2):
+        eng.cf_set_prefill_pairing(mode)
+        out = torch.full((P, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        eng.cf_prefill_attn_varlen(q, cf.pool_of(kp, vp), lens, prefixes, table, out)
+        r0 = 0
+        for i, (l, c, pages) in enumerate(b.chunks):
+            alone = torch.full((l, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+            eng.cf_prefill_attn(q[r0:r0 + l].contiguous(), cf.pool_of(kp, vp), l, c,
+                                torch.as_tensor(pages, device="cuda"), alone)
+            torch.cuda.synchronize()
+            assert torch.equal(out[r0:r0 + l], alone), (mode, i)
+            r0 += l
+    eng.cf_set_prefill_pairing(0)
+    assert eng.cf_get_error()[0] == 0
+
+
+def test_prefill_varlen_rejects_bad_chunks(cf):
+    shape = wl.TINY
+    eng = engine_for(cf, shape)
+    kp = torch.zeros((8, shape.n_kv_heads, 16, shape.head_dim), dtype=torch.bfloat16, device="cuda")
+    pool = cf.pool_of(kp, kp.clone())
+    q = torch.zeros((64, shape.n_q_heads, shape.head_dim), dtype=torch.bfloat16, device="cuda")
+    table = torch.zeros((33, 2), dtype=torch.int32, device="cuda")
+    for lens, prefixes, tb, status in (([0, 5], [0, 0], table[:2], cf.CF_ERR_INVALID_ARG),
+                                       ([5, 5], [-1, 0], table[:2], cf.CF_ERR_INVALID_ARG),
+                                       ([5, 30], [0, 10], table[:2], cf.CF_ERR_INVALID_ARG),   # 3 pages > stride 2
+                                       ([1] * 33, [0] * 33, table, cf.CF_ERR_UNSUPPORTED)):
+        with pytest.raises(cf.CfError) as ex:
+            eng.cf_prefill_attn_varlen(q, pool, lens, prefixes, tb, q)
+        assert ex.value.status == status
+
+
 def test_prefill_equals_decode_for_last_row(cf):
     """The last chunk row sees every key, exactly like a decode query."""
     shape = wl.LLAMA8B

@@ -43,11 +43,17 @@ def bf16_dev(a):
 
 def slots_of_rows(b, rows):
     out = []
+    P = b.prefill_rows
     for r in rows:
-        if r < b.prefill_len:
-            out.append(int(oracle.slot_of(b.pre_pages, b.prefill_prefix + r, 16)))
+        if r < P:
+            r0 = 0
+            for l, c, pages in b.chunks:
+                if r < r0 + l:
+                    out.append(int(oracle.slot_of(pages, c + r - r0, 16)))
+                    break
+                r0 += l
         else:
-            j = r - b.prefill_len
+            j = r - P
             out.append(int(oracle.slot_of(b.dec_pages[j], int(b.dec_ctx[j]), 16)))
     return np.asarray(out, np.int64)
 
@@ -60,7 +66,7 @@ def read_slots(kp, vp, slots):
 def stage_isolated(cf, S, rows=None):
     """Runs each layer stage through the C ABI on the oracle's inputs."""
     b, s, eng, W = S.b, S.s, S.eng, S.W
-    T, l = S.T, b.prefill_len
+    T, l = S.T, b.prefill_rows
     Hq, d, H = s.n_q_heads, s.head_dim, s.hidden
     W64 = S.oracle_weights()
     x64 = f64(S.x)
@@ -95,11 +101,17 @@ def stage_isolated(cf, S, rows=None):
     attn_rows = []
     npre = int(np.sum(need < l))
     if npre:
+        # every chunk's rows at their stacked positions (the rows the oracle
+        # skipped hold zeros: their outputs are not compared)
+        pre_need = torch.as_tensor(need[:npre], device="cuda")
         qp = torch.zeros((l, Hq, d), dtype=torch.bfloat16, device="cuda")
-        qp[:npre] = q_need[:npre]
+        qp[pre_need] = q_need[:npre]
         op = torch.zeros_like(qp)
-        eng.cf_prefill_attn(qp, pool_a, l, b.prefill_prefix, S.pre_pages, op)
-        attn_rows.append(op[:npre])
+        if S.multi:
+            eng.cf_prefill_attn_varlen(qp, pool_a, S.chunk_len, S.chunk_prefix, S.chunk_pages, op)
+        else:
+            eng.cf_prefill_attn(qp, pool_a, l, b.prefill_prefix, S.pre_pages, op)
+        attn_rows.append(op[pre_need])
     dec_sel = need[need >= l] - l
     if len(dec_sel):
         ds = torch.as_tensor(dec_sel, device="cuda")
@@ -168,6 +180,13 @@ SLICES = [
     ("q32b", wl.reduced(wl.WORKLOADS["q32b"], (1000,), 64, 500)),
     ("mix-decode-only", wl.reduced(wl.WORKLOADS["mix"], (700, 20, 3333), 0, 0)),
     ("l8b-prefill-only", wl.reduced(wl.WORKLOADS["l8b"], (), 257, 31)),
+    # several chunks of different requests in one step (ConfluxServe §6.2 Eq. 6)
+    ("tiny-chunks", wl.Workload("tiny-chunks", wl.TINY, 3, (5, 40, 200), 64, 128,
+                                more_chunks=((37, 0), (130, 300), (1, 17)))),
+    ("l8b-chunks", wl.Workload("l8b-chunks", wl.LLAMA8B, 4, (5, 300, 17, 1), 300, 0,
+                               more_chunks=((130, 2000), (129, 700), (1, 5)))),
+    ("q14b-chunks-only", wl.Workload("q14b-chunks-only", wl.QWEN14B, 0, (), 200, 77,
+                                     more_chunks=((64, 0), (257, 1000)))),
 ]
 
 
@@ -182,14 +201,18 @@ def test_layer_chained_parity(cf, name, w):
     chained(LayerSetup(w))
 
 
-FULL = ["l8b", "q14b", "mix", "q32b"]
+FULL = ["l8b", "q14b", "mix", "q32b", "mchunk"]
 
 
 def sample_rows(b):
-    l, nd = b.prefill_len, b.n_decode
+    nd = b.n_decode
     rng = np.random.default_rng(0)
-    return sorted(set([0, 1, min(127, l - 1), min(128, l - 1), l - 1] + list(rng.integers(0, l, 3)) +
-                      [l, l + nd - 1] + list(l + rng.integers(0, nd, 3))))
+    rows, r0 = [], 0
+    for l, _, _ in b.chunks:   # each chunk's first rows, a tile edge, its last row
+        rows += [r0, r0 + 1, r0 + min(127, l - 1), r0 + min(128, l - 1), r0 + l - 1]
+        rows += list(r0 + rng.integers(0, l, 2))
+        r0 += l
+    return sorted(set(int(r) for r in rows + [r0, r0 + nd - 1] + list(r0 + rng.integers(0, nd, 3))))
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -281,6 +304,68 @@ def test_layer_page_permutation_invariance(cf):
     S2.pre_pages.copy_(torch.as_tensor(perm[S2.b.pre_pages], device="cuda"))
     out2 = S2.step()
     assert torch.equal(out1, out2)
+
+
+CHUNKS_W = wl.Workload("l8b-chunks", wl.LLAMA8B, 3, (300, 64, 1000), 96, 40,
+                       more_chunks=((130, 0), (1, 2000), (257, 513)))
+
+
+def test_layer_chunks_match_each_chunk_run_alone(cf):
+    """ConfluxServe §6.2 Eq. 6: several requests' chunks share one step.
+    With the GEMMs' split-K tail off, every chunk's rows are bit-identical
+    to the same chunk run as the only chunk of a step (GEMM rows and
+    attention tiles do not depend on the other rows); decode rows agree
+    within fp32 rounding."""
+    S = LayerSetup(CHUNKS_W)
+    S.eng.cf_set_split_k(1)
+    for pairing in (1, 2):
+        S.eng.cf_set_prefill_pairing(pairing)
+        out = S.step().clone()
+        r0 = 0
+        for i, (l, c, pages) in enumerate(S.b.chunks):
+            xi = S.x[r0:r0 + l].contiguous()
+            oi = torch.empty_like(xi)
+            S.eng.cf_layer_step(cf.batch_of(0, None, None, l, c, torch.as_tensor(pages, device="cuda")), xi, oi,
+                                S.pool)
+            torch.cuda.synchronize()
+            assert torch.equal(oi, out[r0:r0 + l]), (pairing, i)
+            r0 += l
+        xd = S.x[r0:].contiguous()
+        od = torch.empty_like(xd)
+        S.eng.cf_layer_step(cf.batch_of(S.b.n_decode, S.dec_ctx, S.dec_pages, 0, 0, None), xd, od, S.pool)
+        torch.cuda.synchronize()
+        assert S.eng.cf_get_error()[0] == 0
+        assert_close(od, f64(out[r0:]), "decode rows", 1e-2, 1e-3)
+    S.eng.cf_set_prefill_pairing(0)
+    S.eng.cf_set_split_k(0)
+
+
+def test_layer_chunk_list_of_one_equals_the_single_chunk_fields(cf):
+    S = LayerSetup(wl.reduced(wl.WORKLOADS["l8b"], (300, 64), 96, 40))
+    out = S.step().clone()
+    lens, prefixes, table = S.b.chunk_table()
+    b1 = cf.batch_of(S.b.n_decode, S.dec_ctx, S.dec_pages, 0, 0, None,
+                     chunks=(lens, prefixes, torch.as_tensor(table, device="cuda")))
+    o1 = torch.empty_like(out)
+    S.eng.cf_layer_step(b1, S.x, o1, S.pool)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, out)
+
+
+def test_layer_rejects_bad_chunk_lists(cf):
+    S = LayerSetup(CHUNKS_W)
+    lens, prefixes, table = S.b.chunk_table()
+    for bad in (dict(lens=[0] + list(lens[1:])), dict(prefixes=[-1] + list(prefixes[1:])),
+                dict(table=S.chunk_pages[:, :2].contiguous())):
+        args = (bad.get("lens", lens), bad.get("prefixes", prefixes), bad.get("table", S.chunk_pages))
+        b = cf.batch_of(S.b.n_decode, S.dec_ctx, S.dec_pages, 0, 0, None, chunks=args)
+        with pytest.raises(cf.CfError) as ex:
+            S.eng.cf_layer_step(b, S.x, S.out, S.pool)
+        assert ex.value.status == cf.CF_ERR_INVALID_ARG
+    # a single chunk and a chunk list at once
+    b = cf.batch_of(S.b.n_decode, S.dec_ctx, S.dec_pages, 5, 0, S.pre_pages, chunks=(lens, prefixes, S.chunk_pages))
+    with pytest.raises(cf.CfError):
+        S.eng.cf_layer_step(b, S.x, S.out, S.pool)
 
 
 def test_layer_cobatched_rows_match_separate_batches(cf):
@@ -397,6 +482,33 @@ def test_layer_step_graphs_match_eager(cf):
     assert S.eng.cf_graph_captures() == n0 + 1
     assert torch.equal(graph2, eager2)
     assert not torch.equal(eager2, eager)
+    S.eng.cf_set_graphs(False)
+
+
+def test_layer_step_graphs_with_chunk_lists(cf):
+    """Replayed linear segments read the step's chunk table from device
+    memory: another split of the same rows (other prefixes) reuses the
+    captured graphs and still equals the eager step."""
+    S = LayerSetup(CHUNKS_W)
+    out = torch.empty_like(S.x)   # one output buffer: the graphs are keyed on the buffers
+
+    def run(b, graphs):
+        S.eng.cf_set_graphs(graphs)
+        S.eng.cf_layer_step(b, S.x, out, S.pool)
+        torch.cuda.synchronize()
+        assert S.eng.cf_get_error()[0] == 0
+        return out.clone()
+
+    eager = run(S.batch, False)
+    n0 = S.eng.cf_graph_captures()
+    assert torch.equal(run(S.batch, True), eager)
+    lens = S.chunk_len
+    prefixes = S.chunk_prefix // 2
+    b2 = cf.batch_of(S.b.n_decode, S.dec_ctx, S.dec_pages, 0, 0, None, chunks=(lens, prefixes, S.chunk_pages))
+    eager2 = run(b2, False)
+    graph2 = run(b2, True)
+    assert S.eng.cf_graph_captures() == n0 + 1
+    assert torch.equal(graph2, eager2) and not torch.equal(eager2, eager)
     S.eng.cf_set_graphs(False)
 
 
