@@ -427,6 +427,9 @@ def run_kernel_case(args):
     prefill: prefill attention, Qwen3-32B shape, 2048-token chunk on 4096 cached
              (8 query-tile pairs x 64 heads: several waves of paired items)
     gemm   : gate/up GEMM + SwiGLU epilogue of the Llama-3.1-8B layer, T = 1040
+    prefill-chunks: prefill attention over four chunks of different requests in
+             one launch, Llama-3.1-8B shape, (l, c) = (1024, 0), (512, 4096),
+             (256, 12288), (128, 2048)
     """
     import numpy as np
     import torch
@@ -434,11 +437,13 @@ def run_kernel_case(args):
     import co_prefill_decode_gb300 as cf
     import workload as wl
     which = args.kernel
-    s = wl.LLAMA8B if which == "gemm" else wl.QWEN32B
+    s = wl.LLAMA8B if which in ("gemm", "prefill-chunks") else wl.QWEN32B
     if which == "decode":
         w = wl.Workload("k", s, 8, (8192,) * 8, 0, 0)
     elif which == "prefill":
         w = wl.Workload("k", s, 0, (), 2048, 4096)
+    elif which == "prefill-chunks":
+        w = wl.Workload("k", s, 0, (), 1024, 0, more_chunks=((512, 4096), (256, 12288), (128, 2048)))
     else:
         w = wl.Workload("k", s, 0, (), 1040, 0)
     b = wl.make_batch(w, args.seed)
@@ -448,13 +453,13 @@ def run_kernel_case(args):
     pool = cf.pool_of(kp, vp)
     Hq, d = s.n_q_heads, s.head_dim
     g = torch.Generator(device="cuda").manual_seed(args.seed)
-    if which == "prefill":
-        l, cp = b.prefill_len, b.prefill_prefix
-        pos = np.arange(cp, cp + l)
-        pg = torch.as_tensor(b.pre_pages[pos // 16].astype(np.int64), device="cuda")
-        off = torch.as_tensor(pos % 16, device="cuda")
-        kp[pg, :, off, :] = torch.randn(l, s.n_kv_heads, d, device="cuda", generator=g).bfloat16()
-        vp[pg, :, off, :] = torch.randn(l, s.n_kv_heads, d, device="cuda", generator=g).bfloat16()
+    if which in ("prefill", "prefill-chunks"):
+        for l, cp, pages in b.chunks:   # each chunk's own K/V
+            pos = np.arange(cp, cp + l)
+            pg = torch.as_tensor(pages[pos // 16].astype(np.int64), device="cuda")
+            off = torch.as_tensor(pos % 16, device="cuda")
+            kp[pg, :, off, :] = torch.randn(l, s.n_kv_heads, d, device="cuda", generator=g).bfloat16()
+            vp[pg, :, off, :] = torch.randn(l, s.n_kv_heads, d, device="cuda", generator=g).bfloat16()
     for _ in range(2):
         if which == "decode":
             q = torch.randn(b.n_decode, Hq, d, device="cuda", generator=g).bfloat16()
@@ -465,6 +470,11 @@ def run_kernel_case(args):
             q = torch.randn(b.prefill_len, Hq, d, device="cuda", generator=g).bfloat16()
             o = torch.empty_like(q)
             eng.cf_prefill_attn(q, pool, b.prefill_len, b.prefill_prefix, torch.as_tensor(b.pre_pages, device="cuda"), o)
+        elif which == "prefill-chunks":
+            lens, prefixes, table = b.chunk_table()
+            q = torch.randn(b.prefill_rows, Hq, d, device="cuda", generator=g).bfloat16()
+            o = torch.empty_like(q)
+            eng.cf_prefill_attn_varlen(q, pool, lens, prefixes, torch.as_tensor(table, device="cuda"), o)
         else:
             A = torch.randn(1040, s.hidden, device="cuda", generator=g).bfloat16()
             C = torch.empty(1040, s.ffn_dim, device="cuda").bfloat16()
@@ -714,7 +724,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graphs", type=int, default=0, choices=[0, 1],
                     help="replay the linear segments of the step as CUDA graphs (1) or launch eagerly (0)")
-    ap.add_argument("--kernel", choices=["decode", "prefill", "gemm"], default=None,
+    ap.add_argument("--kernel", choices=["decode", "prefill", "gemm", "prefill-chunks"], default=None,
                     help="run one small launch of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--estimator", default=None,
                     help="fit and validate the iteration-latency estimator for these workloads "
