@@ -30,7 +30,7 @@ EXPORTS = (
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
     "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
     "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate", "cf_waterfill_dispatch",
-    "cf_waterfill_assign", "cf_prefill_attn_varlen",
+    "cf_waterfill_assign", "cf_prefill_attn_varlen", "cf_set_prefill_split",
 )
 
 
@@ -130,6 +130,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_set_split_k": (I, [P, I]),
         "cf_selftest_timeout": (I, [P, ctypes.c_ulonglong, P]),
         "cf_set_prefill_pairing": (I, [P, I]),
+        "cf_set_prefill_split": (I, [P, I]),
         "cf_set_graphs": (I, [P, I]),
         "cf_graph_captures": (L, [P]),
         "cf_latency_predict": (I, [ctypes.POINTER(cf_latency_model), I, ctypes.POINTER(cf_rank_load), I,
@@ -305,8 +306,11 @@ class Engine:
         return int(self.lib.cf_graph_captures(self.handle))
 
     def cf_set_prefill_pairing(self, mode: int):
-        """0: automatic, 1: single query tiles, 2: tile pairs sharing each K/V tile."""
+        """0: automatic, 1: single query tiles, 2: tile pairs, 3: head pairs (even GQA groups)."""
         _check(self.lib, self.handle, self.lib.cf_set_prefill_pairing(self.handle, int(mode)))
+
+    def cf_set_prefill_split(self, mode: int):
+        _check(self.lib, self.handle, self.lib.cf_set_prefill_split(self.handle, int(mode)))
 
     def cf_selftest_timeout(self, wait_ns: int, stream=None):
         _check(self.lib, self.handle, self.lib.cf_selftest_timeout(self.handle, int(wait_ns), _stream(stream)))

@@ -126,7 +126,10 @@ struct cf_engine {
   unsigned* counter;             // prefill work queue (set to 0 before each use)
   int* dec_counter;
   int split_mode = 0;            // GEMM split-K tail: 0 automatic, 1 off, >= 2 forced chunk count
-  int prefill_pair = 0;          // prefill items: 0 automatic, 1 single query tiles, 2 tile pairs
+  int prefill_pair = 0;          // prefill items: 0 automatic, 1 single query tiles, 2 tile pairs, 3 head pairs
+  int prefill_split = 0;         // prefill key-range cuts: 0 automatic, 1 never, n >= 2 n ranges
+  float* pf_part_o = nullptr;    // partials of cut prefill items
+  float* pf_part_ml = nullptr;
   float* sk_ws;                  // split-K partial tiles of the GEMMs
   int* sk_flags;                 // their per-tile flags (0 between launches)
   int* err;
@@ -310,8 +313,10 @@ void prefill_chunks_args(cf_engine* e, const StepChunks& ch, PrefillArgs& pf) {
     r += ch.len[i];
   }
   pf.pages = ch.pages;
-  pf.pair = e->prefill_pair ? e->prefill_pair - 1 : prefill_pairing(ch.len, ch.n, pf.Hq, e->sms);
-  prefill_set_chunks(pf, ch.n, ch.len, ch.prefix, row0, off);
+  pf.pair = e->prefill_pair ? e->prefill_pair - 1 : prefill_pairing(ch.len, ch.n, pf.Hq, pf.Hkv, e->sms);
+  pf.part_o = e->pf_part_o;
+  pf.part_ml = e->pf_part_ml;
+  prefill_set_chunks(pf, ch.n, ch.len, ch.prefix, row0, off, e->sms, e->prefill_split);
 }
 
 // RoPE table + slots (and optionally the RMSNorm of x), then the fused QKV
@@ -460,6 +465,7 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   const size_t o_plan = take((size_t)(c.max_decode + 4) * 4), o_cnt = take(4), o_err = take(4);
   const size_t o_dcnt = take(4), o_bdev = take(sizeof(ChunkRows));
   const size_t o_skw = take(gemm_sk_ws_bytes(e->sms)), o_skf = take(gemm_sk_flag_bytes(e->sms));
+  const size_t o_ppo = take((size_t)kPfPartTiles * d * 128 * 4), o_ppml = take((size_t)kPfPartTiles * 128 * 2 * 4);
   e->ws_bytes = off;
   if (cudaMalloc(&e->ws, off) != cudaSuccess) {
     cudaGetLastError();
@@ -485,6 +491,8 @@ cf_status cf_create(const cf_config* cfg, const cf_weights* w, cf_engine** out) 
   e->bdev = reinterpret_cast<ChunkRows*>(b + o_bdev);
   e->sk_ws = reinterpret_cast<float*>(b + o_skw);
   e->sk_flags = reinterpret_cast<int*>(b + o_skf);
+  e->pf_part_o = reinterpret_cast<float*>(b + o_ppo);
+  e->pf_part_ml = reinterpret_cast<float*>(b + o_ppml);
   bool ok = cudaMemset(e->ws, 0, off) == cudaSuccess;
   // RoPE inverse frequencies theta^(-2i/d), in double
   std::vector<double> inv(d / 2);
@@ -796,6 +804,10 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     e->launches++;
     CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_join, 0));
   }
+  if (l > 0 && prefill_merge_blocks(pf) > 0) {   // both prefill grids are done: merge the cut items
+    CF_CUDA(e, launch_prefill_merge(pf, s));
+    e->launches++;
+  }
   if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_JOIN], s));
 
   // a6 - a9
@@ -917,6 +929,10 @@ cf_status prefill_attn_impl(cf_engine* e, const void* q, const cf_kv_pool* pool,
   pf.wait_ns = kWaitNs;
   CF_CUDA(e, launch_prefill(tq, e->pm.tk, e->pm.tv, pf, ctas, s));
   e->launches++;
+  if (prefill_merge_blocks(pf) > 0) {
+    CF_CUDA(e, launch_prefill_merge(pf, s));
+    e->launches++;
+  }
   return CF_OK;
 }
 
@@ -1013,8 +1029,15 @@ cf_status cf_gemm_schedule(int M, int N, int K, int epilogue, int ctas, int spli
 }
 
 cf_status cf_set_prefill_pairing(cf_engine* e, int mode) {
-  if (!e || mode < 0 || mode > 2) return CF_ERR_INVALID_ARG;
+  if (!e || mode < 0 || mode > 3) return CF_ERR_INVALID_ARG;
+  if (mode == 3 && (e->cfg.n_q_heads / e->cfg.n_kv_heads) % 2) return fail(e, CF_ERR_UNSUPPORTED, "odd GQA group");
   e->prefill_pair = mode;
+  return CF_OK;
+}
+
+cf_status cf_set_prefill_split(cf_engine* e, int mode) {
+  if (!e || mode < 0 || mode > kPfMaxSplits) return CF_ERR_INVALID_ARG;
+  e->prefill_split = mode;
   return CF_OK;
 }
 

@@ -181,16 +181,29 @@ cudaError_t launch_decode_kernel(const CUtensorMap& tmK, const CUtensorMap& tmV,
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------------ prefill attention
+// Query tiles of a prefill work item (pair kinds): one (query tile, head);
+// two consecutive query tiles of one head; or one query tile of two heads
+// that read the same KV head (GQA groups of even size).
+constexpr int kPfSingle = 0, kPfTilePairs = 1, kPfHeadPairs = 2;
+constexpr int kPfMaxSplits = 16;
+constexpr int kPfPartTiles = 512;   // fp32 partial (query tile) slots of split items per engine
+
 struct PrefillArgs {
   // Work items are numbered chunk slot by chunk slot (slots sorted so that the
   // chunk reaching furthest into its request comes first); slot s owns items
-  // [item_end[s-1], item_end[s]).
+  // [item_end[s-1], item_end[s]).  A slot's units (tile or tile pair) are cut
+  // into splits[s] key ranges each (1: not cut); item = unit * splits + split.
   int n_chunks;
   int item_end[kMaxChunks];
   int row0[kMaxChunks];           // the chunk's first row of Q and of out
   int len[kMaxChunks];            // l_i
   int prefix[kMaxChunks];         // c_i
   int page_off[kMaxChunks];       // its page table: pages + page_off, ceil((c_i + l_i) / ps) ids
+  int splits[kMaxChunks];
+  int part_base[kMaxChunks];      // first partial slot of the slot's split items (2 per item: A, B)
+  int merge_end[kMaxChunks];      // merge blocks of slots 0..s (2 per unit of a cut slot)
+  float* part_o;                  // [kPfPartTiles][D][128] unnormalised O of a split's query tile
+  float* part_ml;                 // [kPfPartTiles][128][2] its running max (log2 units) and sum
   int Hq, Hkv, head_dim, page_size, num_pages;
   const int* pages;
   __nv_bfloat16* out;             // row i at out + i * out_stride, [Hq][d]
@@ -199,22 +212,31 @@ struct PrefillArgs {
   unsigned* counter;              // work queue shared by the launches of one step
   unsigned base;                  // counter value at the start of this launch's queue (0)
   int pdl;                        // as DecodeArgs::pdl
-  int pair;                       // items are pairs of query tiles sharing each K/V tile (1) or single
-                                  // tiles (0); every grid draining one queue must agree
+  int pair;                       // kPfSingle / kPfTilePairs / kPfHeadPairs; every grid draining one
+                                  // queue must agree
   int* err;
   unsigned long long wait_ns;
 };
-// Pair query tiles when that still leaves at least one item per SM of the device.
-inline int prefill_pairing(const int* len, int n, int Hq, int sms) {
+// The pair kind of a launch: two heads of one KV head when the GQA group
+// size is even; otherwise pairs of query tiles when that still leaves one
+// item per SM of the device, else single tiles.
+inline int prefill_pairing(const int* len, int n, int Hq, int Hkv, int sms) {
+  if ((Hq / Hkv) % 2 == 0) return kPfHeadPairs;
   long long groups = 0;
   for (int i = 0; i < n; ++i) groups += ((len[i] + 127) / 128 + 1) / 2;
-  return groups * Hq >= sms ? 1 : 0;
+  return groups * Hq >= sms ? kPfTilePairs : kPfSingle;
 }
-// Fills the chunk slots and item counts of `a` (a.Hq and a.pair set) from
-// chunks given in stacked-row order: lengths, prefixes, first rows and page
-// table offsets.
+// Fills the chunk slots, splits and item counts of `a` (a.Hq, a.Hkv and
+// a.pair set) from chunks given in stacked-row order: lengths, prefixes,
+// first rows and page table offsets.  split_mode 0 cuts the key range of a
+// chunk's items when they would otherwise be the launch's critical path
+// (longer than the average work per SM of `sms` CTAs); 1 never cuts; n >= 2
+// cuts every chunk into n ranges where it can (at most its shortest item's
+// key tiles, kPfMaxSplits, and the partial slots).
 void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix, const int* row0,
-                        const int* page_off);
+                        const int* page_off, int sms, int split_mode);
+// Merge blocks of a launch (0: no cut items).
+int prefill_merge_blocks(const PrefillArgs& a);
 
 // CTAs a launch really uses (<= items), and the items of a launch.
 int prefill_grid(const PrefillArgs& a, int num_ctas);
@@ -223,6 +245,9 @@ int prefill_items(const PrefillArgs& a);
 // tmK/tmV: 2-D {d, pages*Hkv*ps} over the pools with box {64, 16}.
 cudaError_t launch_prefill(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const PrefillArgs& a, int num_ctas, cudaStream_t s);
+// Combines the partials of cut items into the output (after every grid of
+// the launch is done); does nothing when no item was cut.
+cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s);
 
 int device_sm_count();
 

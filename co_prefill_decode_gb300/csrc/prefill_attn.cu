@@ -37,6 +37,9 @@
 // tensor core computes tile B's products while tile A's softmax runs and the
 // other way round, so the two softmax groups alternate on the exp units and
 // the tensor pipe stays busy.
+#include <algorithm>
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -68,33 +71,64 @@ struct PfCfg {
 };
 
 struct Item {
-  int qa, qb, head;   // query tiles A and B (qb = -1: none) of the chunk
+  int qa, ha, qb, hb;   // query tile and head of tiles A and B (qb = -1: no tile B)
+  int k0, k1;           // the key tiles [k0, k1) this item visits
+  int part;             // partial slot of tile A (B: part + 1) of a cut item; -1: not cut
   int row0, len, prefix;
-  const int* pages;   // the chunk's page table
+  const int* pages;     // the chunk's page table
 };
 
-// Item idx: its chunk slot, then within the slot pairs of tiles (pair) or
-// tiles, heaviest (last) query tiles first, query head fastest.
-CF_DEV Item item_at(const PrefillArgs& a, int idx) {
-  int sl = 0;
-  while (sl + 1 < a.n_chunks && a.item_end[sl] <= idx) ++sl;
-  const int local = idx - (sl ? a.item_end[sl - 1] : 0);
-  Item it;
-  it.row0 = a.row0[sl];
-  it.len = a.len[sl];
-  it.prefix = a.prefix[sl];
-  it.pages = a.pages + a.page_off[sl];
-  const int n_qt = (it.len + BQ - 1) / BQ;
-  const int n_groups = a.pair ? (n_qt + 1) / 2 : n_qt;
-  const int g = n_groups - 1 - local / a.Hq;
-  it.head = local % a.Hq;
-  it.qa = a.pair ? 2 * g : g;
-  it.qb = (a.pair && 2 * g + 1 < n_qt) ? 2 * g + 1 : -1;
-  return it;
+__host__ __device__ inline int units_of(int kind, int n_qt, int Hq) {
+  return kind == kPfHeadPairs ? n_qt * (Hq / 2) : (kind == kPfTilePairs ? (n_qt + 1) / 2 : n_qt) * Hq;
+}
+// Unit u of a chunk with n_qt query tiles, heaviest (last) query tiles
+// first, heads fastest (heads of one KV head adjacent).
+CF_DEV void unit_tiles(int kind, int u, int n_qt, int Hq, Item& it) {
+  if (kind == kPfHeadPairs) {
+    const int hp = Hq / 2;
+    it.qa = it.qb = n_qt - 1 - u / hp;
+    it.ha = 2 * (u % hp);
+    it.hb = it.ha + 1;
+  } else {
+    const int n_groups = kind == kPfTilePairs ? (n_qt + 1) / 2 : n_qt;
+    const int g = n_groups - 1 - u / Hq;
+    it.ha = it.hb = u % Hq;
+    it.qa = kind == kPfTilePairs ? 2 * g : g;
+    it.qb = (kind == kPfTilePairs && 2 * g + 1 < n_qt) ? 2 * g + 1 : -1;
+  }
 }
 CF_DEV int kv_tiles(const Item& it, int qt) {
   const int end = min(it.prefix + qt * BQ + BQ, it.prefix + it.len);   // exclusive key end
   return (end + BKV - 1) / BKV;
+}
+CF_DEV int slot_of(const PrefillArgs& a, int idx) {
+  int sl = 0;
+  while (sl + 1 < a.n_chunks && a.item_end[sl] <= idx) ++sl;
+  return sl;
+}
+CF_DEV void chunk_of(const PrefillArgs& a, int sl, Item& it) {
+  it.row0 = a.row0[sl];
+  it.len = a.len[sl];
+  it.prefix = a.prefix[sl];
+  it.pages = a.pages + a.page_off[sl];
+}
+
+// Item idx: its chunk slot, its unit and its key range.  Split s of S covers
+// key tiles [s r / S, (s+1) r / S) of the unit's reach r (the key tiles of
+// its later query tile).
+CF_DEV Item item_at(const PrefillArgs& a, int idx) {
+  const int sl = slot_of(a, idx);
+  const int local = idx - (sl ? a.item_end[sl - 1] : 0);
+  Item it;
+  chunk_of(a, sl, it);
+  const int S = a.splits[sl];
+  const int u = local / S, sp = local % S;
+  unit_tiles(a.pair, u, (it.len + BQ - 1) / BQ, a.Hq, it);
+  const int reach = kv_tiles(it, it.qb > it.qa ? it.qb : it.qa);
+  it.k0 = sp * reach / S;
+  it.k1 = (sp + 1) * reach / S;
+  it.part = S > 1 ? a.part_base[sl] + 2 * local : -1;
+  return it;
 }
 
 template <int D>
@@ -200,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int t = 0; t < nq; ++t)
 #pragma unroll
                 for (int hd = 0; hd < D / 64; ++hd)
-                  tma_load_3d(smem + C::OFF_Q + t * C::TILE + hd * C::HALF, &tmQ, q_full, hd * 64, it0.head,
-                              it0.row0 + (t ? it0.qb : it0.qa) * BQ);
+                  tma_load_3d(smem + C::OFF_Q + t * C::TILE + hd * C::HALF, &tmQ, q_full, hd * 64,
+                              t ? it0.hb : it0.ha, it0.row0 + (t ? it0.qb : it0.qa) * BQ);
               last_q = qc & 1;
             }
           }
@@ -214,12 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       idx = __shfl_sync(0xffffffffu, idx, 0);
       if (!ok || idx < 0) break;
       const Item it = item_at(a, idx);
-      const int kvh = it.head / G;
+      const int kvh = it.ha / G;   // tile B's head reads the same KV head
       ++qc;
-      const int nkv = kv_tiles(it, it.qb >= 0 ? it.qb : it.qa);   // the later tile reaches furthest
       const int n_pages_req = (it.prefix + it.len + a.page_size - 1) / a.page_size;
-      int pid = (lane < 8 && lane < n_pages_req) ? it.pages[lane] : -1;
-      for (int j = 0; j < nkv; ++j, ++kc) {
+      int pid = (lane < 8 && it.k0 * 8 + lane < n_pages_req) ? it.pages[it.k0 * 8 + lane] : -1;
+      for (int j = it.k0; j < it.k1; ++j, ++kc) {
         const int st = kc % NS;
         const uint32_t ph = (kc / NS) & 1;
         const int pi = j * 8 + lane;
@@ -232,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // page ids of the next tile, so the next copies do not wait on them
         const int pin = (j + 1) * 8 + lane;
-        const int pid_next = (lane < 8 && j + 1 < nkv && pin < n_pages_req) ? it.pages[pin] : -1;
+        const int pid_next = (lane < 8 && j + 1 < it.k1 && pin < n_pages_req) ? it.pages[pin] : -1;
         const int my_page = lane / (D / 64), my_hd = lane % (D / 64);
         const int my_row = __shfl_sync(0xffffffffu, row, my_page & 7);
         uint64_t* full = is_v ? &v_full[st] : &k_full[st];
@@ -301,38 +334,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int idx = ring[k & 7];
         if (idx < 0) break;
         const Item it = item_at(a, idx);
-        int nt[2];
-        nt[0] = kv_tiles(it, it.qa);
-        nt[1] = it.qb >= 0 ? kv_tiles(it, it.qb) : 0;
-        const int n = nt[0] > nt[1] ? nt[0] : nt[1];
+        // the key tiles of query tile x in this item end at e[x] (none if e[x] <= k0)
+        int e[2];
+        e[0] = min(it.k1, kv_tiles(it, it.qa));
+        e[1] = it.qb >= 0 ? min(it.k1, kv_tiles(it, it.qb)) : 0;
+        const int k0 = it.k0, n = it.k1;
         if (!mbar_wait(q_full, qc & 1, wc)) { ok = false; break; }
         ++qc;
-        // S of key tile 0 for both query tiles
+        // S of key tile k0 for both query tiles
         if (!mbar_wait(&k_full[kc % NS], (kc / NS) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
-          if (nt[x] > 0) issue_s(x, kc % NS);
+          if (e[x] > k0) issue_s(x, kc % NS);
         umma_commit(&k_empty[kc % NS]);
         ++kc;
-        if (n == 1) umma_commit(q_empty);
-        for (int j = 0; j < n && ok; ++j) {
+        if (n - k0 == 1) umma_commit(q_empty);
+        for (int j = k0; j < n && ok; ++j) {
           const int vst = vc % NS;
           if (!mbar_wait(&v_full[vst], (vc / NS) & 1, wc)) { ok = false; break; }
           const bool more = j + 1 < n;
           bool k_ready = false;
           for (int x = 0; x < 2 && ok; ++x) {
-            if (j < nt[x]) {   // O_x += P_x(j) V_j
+            if (j < e[x]) {   // O_x += P_x(j) V_j
               if (!mbar_wait(&p_full[x], pc[x] & 1, wc)) { ok = false; break; }
               ++pc[x];
-              if (j == 0) {   // the previous item's epilogue has read O_x
+              if (j == k0) {   // the previous item's epilogue has read O_x
                 if (!mbar_wait(&o_free[x], (ofc[x] & 1) ^ 1, wc)) { ok = false; break; }
                 ++ofc[x];
               }
               tc_fence_after();
-              issue_pv(x, vst, j == 0);
-              if (j == nt[x] - 1) umma_commit(&o_done[x]);
+              issue_pv(x, vst, j == k0);
+              if (j == e[x] - 1) umma_commit(&o_done[x]);
             }
-            if (more && j + 1 < nt[x]) {   // S_x(j+1): overwrites P_x(j) after the PV above has read it
+            if (more && j + 1 < e[x]) {   // S_x(j+1): overwrites P_x(j) after the PV above has read it
               if (!k_ready) {
                 if (!mbar_wait(&k_full[kc % NS], (kc / NS) & 1, wc)) { ok = false; break; }
                 tc_fence_after();
@@ -373,15 +407,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < 0) break;
       const Item it = item_at(a, idx);
       const int qt = x ? it.qb : it.qa;
-      const int na = kv_tiles(it, it.qa);
-      const int nx = qt >= 0 ? kv_tiles(it, qt) : 0;
-      const int n = it.qb >= 0 ? kv_tiles(it, it.qb) : na;   // key tiles of the item
+      const int ea = min(it.k1, kv_tiles(it, it.qa));                  // tile A's key tiles end here
+      const int ex = qt >= 0 ? min(it.k1, kv_tiles(it, qt)) : it.k0;   // this tile's
       const int qi = qt * BQ + r;               // query row within the chunk
       const int qpos = it.prefix + qi;
       const int kend = it.prefix + it.len;      // first key that does not exist
       const int diag = it.prefix + qt * BQ;     // smallest query position of the tile
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nx; ++j) {
+      for (int j = it.k0; j < ex; ++j) {
         if (!mbar_wait(&s_full[x], sc & 1, wc)) { ok = false; break; }
         ++sc;
         tc_fence_after();
@@ -446,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Keys past the end of the request: zero their V rows (the slots may
         // hold anything).  The tile whose PV reads V_j first does it: A while
         // it has key tile j, else B.
-        const int vcnt = vbase + j;
-        if (kend - kv0 < BKV && (x == 0 || j >= na)) {
+        const int vcnt = vbase + (j - it.k0);
+        if (kend - kv0 < BKV && (x == 0 || j >= ea)) {
           const int vst = vcnt % NS;
           if (!mbar_wait(&v_full[vst], (vcnt / NS) & 1, wc)) ok = false;
           const int vk = max(0, kend - kv0);
@@ -466,17 +499,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&p_full[x]);
         if (!ok) break;
       }
-      vbase += n;
-      if (!ok || nx == 0) continue;
-      // epilogue: O / l -> bf16
+      vbase += it.k1 - it.k0;
+      if (!ok) continue;
+      if (ex <= it.k0) {   // no key tile of this query tile in the item
+        if (qt >= 0 && it.part >= 0)
+          reinterpret_cast<float2*>(a.part_ml)[(size_t)(it.part + x) * BQ + r] = make_float2(-INFINITY, 0.f);
+        continue;
+      }
       if (!mbar_wait(&o_done[x], odc & 1, wc)) {
         ok = false;
         break;
       }
       ++odc;
       tc_fence_after();
+      if (it.part >= 0) {
+        // a cut item: unnormalised O and (m, l) of this key range, merged later;
+        // partial slot P holds O column-major [D][128] so a warp writes 128 B rows
+        const size_t P = (size_t)(it.part + x);
+        reinterpret_cast<float2*>(a.part_ml)[P * BQ + r] = make_float2(m, l);
+        float* po = a.part_o + P * D * BQ + r;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(to + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) po[(size_t)(c * 32 + i) * BQ] = o[i];
+        }
+        tc_fence_before();
+        mbar_arrive(&o_free[x]);
+        continue;
+      }
+      // epilogue: O / l -> bf16
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      __nv_bfloat16* orow = a.out + (size_t)(it.row0 + qi) * a.out_stride + (size_t)it.head * D;
+      __nv_bfloat16* orow = a.out + (size_t)(it.row0 + qi) * a.out_stride + (size_t)(x ? it.hb : it.ha) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
@@ -506,6 +562,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// One CTA per query tile of a cut unit, one thread per query row: the
+// partials of the unit's key ranges, each (O_s, m_s, l_s) with
+// O_s = sum exp2(s - m_s) v, combine as
+// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M = max m_s,
+// in split order (deterministic).
+template <int D>
+__global__ void __launch_bounds__(BQ) prefill_merge_kernel(const __grid_constant__ PrefillArgs a) {
+  const int b = blockIdx.x, r = threadIdx.x;
+  int sl = 0;
+  while (sl + 1 < a.n_chunks && a.merge_end[sl] <= b) ++sl;
+  const int local = b - (sl ? a.merge_end[sl - 1] : 0);
+  const int u = local >> 1, x = local & 1;
+  Item it;
+  chunk_of(a, sl, it);
+  unit_tiles(a.pair, u, (it.len + BQ - 1) / BQ, a.Hq, it);
+  const int qt = x ? it.qb : it.qa;
+  if (qt < 0) return;
+  const int qi = qt * BQ + r;
+  if (qi >= it.len) return;
+  const int S = a.splits[sl];
+  const int P0 = a.part_base[sl] + 2 * u * S + x;   // split s at P0 + 2 s
+  float w[kPfMaxSplits];
+  float M = -INFINITY, L = 0.f;
+  for (int sp = 0; sp < S; ++sp) {
+    const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[(size_t)(P0 + 2 * sp) * BQ + r];
+    w[sp] = ml.y > 0.f ? ml.x : -INFINITY;
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  for (int sp = 0; sp < S; ++sp) {
+    const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[(size_t)(P0 + 2 * sp) * BQ + r];
+    w[sp] = w[sp] == -INFINITY ? 0.f : fast_exp2(w[sp] - M);
+    L += w[sp] * ml.y;
+  }
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+  __nv_bfloat16* orow = a.out + (size_t)(it.row0 + qi) * a.out_stride + (size_t)(x ? it.hb : it.ha) * D;
+#pragma unroll 1
+  for (int c = 0; c < D; c += 8) {
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = 0.f;
+    for (int sp = 0; sp < S; ++sp) {
+      if (w[sp] == 0.f) continue;
+      const float* po = a.part_o + (size_t)(P0 + 2 * sp) * D * BQ + r;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = fmaf(w[sp], po[(size_t)(c + i) * BQ], o[i]);
+    }
+    uint4 v;
+    v.x = pack_bf16(o[0] * inv, o[1] * inv);
+    v.y = pack_bf16(o[2] * inv, o[3] * inv);
+    v.z = pack_bf16(o[4] * inv, o[5] * inv);
+    v.w = pack_bf16(o[6] * inv, o[7] * inv);
+    *reinterpret_cast<uint4*>(orow + c) = v;
+  }
+}
+
 template <int D>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const PrefillArgs& a,
                      int ctas, cudaStream_t s) {
@@ -526,8 +637,17 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
 
 int prefill_items(const PrefillArgs& a) { return a.n_chunks > 0 ? a.item_end[a.n_chunks - 1] : 0; }
 
+int prefill_merge_blocks(const PrefillArgs& a) { return a.n_chunks > 0 ? a.merge_end[a.n_chunks - 1] : 0; }
+
+namespace {
+int kv_tiles_host(int prefix, int len, int qt) {
+  const int end = std::min(prefix + qt * BQ + BQ, prefix + len);
+  return (end + BKV - 1) / BKV;
+}
+}  // namespace
+
 void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix, const int* row0,
-                        const int* page_off) {
+                        const int* page_off, int sms, int split_mode) {
   // slot order: the chunk whose last query tile reaches furthest (most key
   // tiles per item) first, so the queue hands out the longest items first
   int order[kMaxChunks];
@@ -538,13 +658,49 @@ void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix
       order[j] = order[j - 1];
       order[j - 1] = t;
     }
+  // per unit the key tiles of its later query tile: the work of the launch
+  // and the longest and shortest unit of each chunk
+  long long total = 0;
+  int reach_max[kMaxChunks], reach_min[kMaxChunks], units[kMaxChunks];
+  for (int i = 0; i < n; ++i) {
+    const int n_qt = (len[i] + BQ - 1) / BQ;
+    units[i] = units_of(a.pair, n_qt, a.Hq);
+    long long cost = 0;
+    if (a.pair == kPfTilePairs) {
+      for (int g = 0; g < (n_qt + 1) / 2; ++g) cost += kv_tiles_host(prefix[i], len[i], std::min(2 * g + 1, n_qt - 1));
+      cost *= a.Hq;
+      reach_min[i] = kv_tiles_host(prefix[i], len[i], std::min(1, n_qt - 1));
+    } else {
+      for (int qt = 0; qt < n_qt; ++qt) cost += kv_tiles_host(prefix[i], len[i], qt);
+      cost *= a.pair == kPfHeadPairs ? a.Hq / 2 : a.Hq;
+      reach_min[i] = kv_tiles_host(prefix[i], len[i], 0);
+    }
+    reach_max[i] = kv_tiles_host(prefix[i], len[i], n_qt - 1);
+    total += cost;
+  }
+  const double avg = (double)total / (sms > 0 ? sms : 1);
+  const double target = avg > 8.0 ? avg : 8.0;   // shortest range worth a split of its own
   a.n_chunks = n;
-  int items = 0;
+  int items = 0, parts = 0, merges = 0;
   for (int s = 0; s < n; ++s) {
     const int i = order[s];
-    const int n_qt = (len[i] + BQ - 1) / BQ;
-    items += (a.pair ? (n_qt + 1) / 2 : n_qt) * a.Hq;
+    int S = 1;
+    if (split_mode >= 2)
+      S = split_mode;
+    else if (split_mode == 0 && reach_max[i] > 1.25 * target)
+      S = (int)std::ceil(reach_max[i] / target);
+    S = std::min(S, std::min(reach_min[i], kPfMaxSplits));   // every split has a key tile
+    if (S > 1 && parts + 2 * units[i] * S > kPfPartTiles) S = (kPfPartTiles - parts) / (2 * units[i]);
+    if (S < 2) S = 1;
+    a.splits[s] = S;
+    a.part_base[s] = S > 1 ? parts : -1;
+    if (S > 1) {
+      parts += 2 * units[i] * S;
+      merges += 2 * units[i];
+    }
+    items += units[i] * S;
     a.item_end[s] = items;
+    a.merge_end[s] = merges;
     a.row0[s] = row0[i];
     a.len[s] = len[i];
     a.prefix[s] = prefix[i];
@@ -564,6 +720,18 @@ cudaError_t launch_prefill(const CUtensorMap& tmQ, const CUtensorMap& tmK, const
   if (a.head_dim == 128) return launch_t<128>(tmQ, tmK, tmV, a, num_ctas, s);
   if (a.head_dim == 64) return launch_t<64>(tmQ, tmK, tmV, a, num_ctas, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s) {
+  const int blocks = prefill_merge_blocks(a);
+  if (blocks <= 0) return cudaSuccess;
+  if (a.head_dim == 128)
+    prefill_merge_kernel<128><<<blocks, BQ, 0, s>>>(a);
+  else if (a.head_dim == 64)
+    prefill_merge_kernel<64><<<blocks, BQ, 0, s>>>(a);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 }  // namespace cf

@@ -135,11 +135,30 @@ cf_status cf_set_graphs(cf_engine* e, int enable);
 /* Number of graph pairs this engine has captured so far. */
 long long cf_graph_captures(cf_engine* e);
 
-/* Work items of prefill attention: 0 (default) pairs consecutive 128-row
- * query tiles of a head, which share every K/V tile, when the chunk has at
- * least one such pair per SM, else uses single tiles; 1 always single
- * tiles; 2 always pairs.  Outputs are the same bits in every mode. */
+/* Work items of prefill attention.  Each item runs two 128-row query tiles
+ * that share every K/V tile it loads, or one:
+ *   1 single tiles;
+ *   2 two consecutive query tiles of one head;
+ *   3 one query tile of two heads of the same KV head (GQA groups of even
+ *     size only; CF_ERR_UNSUPPORTED otherwise);
+ *   0 (default) 3 when the group size is even, else 2 when the chunks have
+ *     at least one tile pair per SM, else 1.
+ * A query tile is computed the same way in every mode (same key order, same
+ * products), so outputs are the same bits in every mode. */
 cf_status cf_set_prefill_pairing(cf_engine* e, int mode);
+/* Key-range cuts of prefill items (flash-decoding style, for items that
+ * would otherwise be the critical path of a launch: a short chunk after a
+ * long prefix gives few, long items).  A cut item covers a range of key
+ * tiles and writes its unnormalised output, running max and sum (fp32) to
+ * engine workspace; a merge kernel combines the ranges in order, so results
+ * are deterministic.  0 (default): cut a chunk's items into
+ * ceil(reach / w) ranges when its longest item reaches more than 1.25 w key
+ * tiles, w the launch's average key tiles per SM (at least 8); 1 never; n in
+ * 2..16 cut every chunk into n ranges where possible.  A chunk is cut into
+ * at most as many ranges as its shortest item has key tiles, and cut items
+ * use at most 512 partial tiles per launch.  Cut rows agree with uncut ones
+ * within fp32 rounding. */
+cf_status cf_set_prefill_split(cf_engine* e, int mode);
 
 /* Failure-detection self-test (no counterpart on the pages): launches one
  * 128 x 256 GEMM tile on the engine's own buffers whose MMA-issuing thread

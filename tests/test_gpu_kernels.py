@@ -261,9 +261,18 @@ PREFILL_CASES = [
 ]
 
 
+def pairing_modes(shape):
+    """Prefill pair kinds valid for the shape: automatic, single tiles, tile
+    pairs, and head pairs when the GQA group size is even."""
+    return [0, 1, 2] + ([3] if (shape.n_q_heads // shape.n_kv_heads) % 2 == 0 else [])
+
+
 @pytest.mark.parametrize("name,shape,l,cp", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
-@pytest.mark.parametrize("pairing", [0, 2])
-def test_prefill_attention_matches_oracle(cf, name, shape, l, cp, pairing):
+@pytest.mark.parametrize("pairing", [0, 2, 3])
+@pytest.mark.parametrize("split", [0, 1, 3])
+def test_prefill_attention_matches_oracle(cf, name, shape, l, cp, pairing, split):
+    if pairing not in pairing_modes(shape):
+        pytest.skip("head pairs need an even GQA group")
     w = wl.Workload(name, shape, 0, (), l, cp)
     b = wl.make_batch(w, 4)
     kp, vp = wl.make_pools(w, b, 4, "cuda")
@@ -272,7 +281,8 @@ def test_prefill_attention_matches_oracle(cf, name, shape, l, cp, pairing):
     q = randn_bf16((l, Hq, d), 14)
     out = torch.zeros((l, Hq, d), dtype=torch.bfloat16, device="cuda")
     eng = engine_for(cf, shape)
-    eng.cf_set_prefill_pairing(pairing)   # automatic (single tiles at these sizes), or tile pairs
+    eng.cf_set_prefill_pairing(pairing)
+    eng.cf_set_prefill_split(split)       # automatic, never, or 3 key ranges where possible
     ref = oracle.prefill_attention(f64(q), kp, vp, cp, b.pre_pages, 16)
     eng.cf_prefill_attn(q, cf.pool_of(kp, vp), l, cp, torch.as_tensor(b.pre_pages, device="cuda"), out)
     torch.cuda.synchronize()
@@ -291,9 +301,10 @@ def test_prefill_pairs_change_no_bit(cf, name, shape, l, cp):
     q = randn_bf16((l, Hq, d), 41)
     fill_positions(kp, vp, b.pre_pages, cp, l, 42)
     eng = engine_for(cf, shape)
+    eng.cf_set_prefill_split(1)
     pages = torch.as_tensor(b.pre_pages, device="cuda")
     outs = []
-    for mode in (1, 2):
+    for mode in pairing_modes(shape)[1:]:
         eng.cf_set_prefill_pairing(mode)
         o = torch.full((l, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
         eng.cf_prefill_attn(q, cf.pool_of(kp, vp), l, cp, pages, o)
@@ -301,7 +312,56 @@ def test_prefill_pairs_change_no_bit(cf, name, shape, l, cp):
     eng.cf_set_prefill_pairing(0)
     torch.cuda.synchronize()
     assert eng.cf_get_error()[0] == 0
-    assert torch.equal(outs[0], outs[1])
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+
+
+SPLIT_CASES = [
+    ("l8b-short-after-long", wl.LLAMA8B, 123, 8082),
+    ("l8b-two-tiles", wl.LLAMA8B, 256, 3000),
+    ("q14b-odd-group", wl.QWEN14B, 200, 5000),
+    ("tiny", wl.TINY, 77, 700),
+]
+
+
+@pytest.mark.parametrize("name,shape,l,cp", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_prefill_key_range_cuts_agree_with_uncut(cf, name, shape, l, cp):
+    """Items cut into key ranges (partials merged in order) agree with the
+    uncut items within fp32 rounding, in every pair kind; the automatic
+    policy cuts a short chunk after a long prefix; repeated runs are
+    bit-identical."""
+    w = wl.Workload(name, shape, 0, (), l, cp)
+    b = wl.make_batch(w, 8)
+    kp, vp = wl.make_pools(w, b, 8, "cuda")
+    fill_positions(kp, vp, b.pre_pages, cp, l, 80)
+    Hq, d = shape.n_q_heads, shape.head_dim
+    q = randn_bf16((l, Hq, d), 18)
+    eng = engine_for(cf, shape)
+    pages = torch.as_tensor(b.pre_pages, device="cuda")
+    ref = oracle.prefill_attention(f64(q), kp, vp, cp, b.pre_pages, 16)
+
+    def run(pairing, split):
+        eng.cf_set_prefill_pairing(pairing)
+        eng.cf_set_prefill_split(split)
+        o = torch.full((l, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        eng.cf_prefill_attn(q, cf.pool_of(kp, vp), l, cp, pages, o)
+        torch.cuda.synchronize()
+        assert eng.cf_get_error()[0] == 0
+        return o
+
+    for pairing in pairing_modes(shape):
+        uncut = run(pairing, 1)
+        for split in (0, 2, 5, 16):
+            o = run(pairing, split)
+            assert_close(o, f64(uncut), f"{name} pairing {pairing} split {split} vs uncut", 1e-2, 1e-3)
+            assert_close(o, ref, f"{name} pairing {pairing} split {split}")
+            assert torch.equal(o, run(pairing, split))
+    n0 = eng.cf_launch_count()
+    run(0, 0)
+    cut = eng.cf_launch_count() - n0 == 2    # prefill + merge
+    assert cut == (name != "tiny")   # tiny: 2 short units, nothing to balance
+    eng.cf_set_prefill_pairing(0)
+    eng.cf_set_prefill_split(0)
 
 
 # several chunks of different requests in one launch (ConfluxServe §6.2
@@ -326,8 +386,11 @@ def varlen_setup(shape, chunks, seed):
 
 
 @pytest.mark.parametrize("name,shape,chunks", VARLEN_CASES, ids=[c[0] for c in VARLEN_CASES])
-@pytest.mark.parametrize("pairing", [0, 1, 2])
-def test_prefill_varlen_matches_oracle(cf, name, shape, chunks, pairing):
+@pytest.mark.parametrize("pairing", [0, 1, 2, 3])
+@pytest.mark.parametrize("split", [0, 4])
+def test_prefill_varlen_matches_oracle(cf, name, shape, chunks, pairing, split):
+    if pairing not in pairing_modes(shape):
+        pytest.skip("head pairs need an even GQA group")
     b, kp, vp, lens, prefixes, table = varlen_setup(shape, chunks, 6)
     Hq, d = shape.n_q_heads, shape.head_dim
     P = int(lens.sum())
@@ -335,10 +398,12 @@ def test_prefill_varlen_matches_oracle(cf, name, shape, chunks, pairing):
     out = torch.full((P, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     eng = engine_for(cf, shape)
     eng.cf_set_prefill_pairing(pairing)
+    eng.cf_set_prefill_split(split)
     eng.cf_prefill_attn_varlen(q, cf.pool_of(kp, vp), lens, prefixes, table, out)
     torch.cuda.synchronize()
     assert eng.cf_get_error()[0] == 0
     eng.cf_set_prefill_pairing(0)
+    eng.cf_set_prefill_split(0)
     r0 = 0
     for l, c, pages in b.chunks:
         ref = oracle.prefill_attention(f64(q[r0:r0 + l]), kp, vp, c, pages, 16)
@@ -355,7 +420,8 @@ def test_prefill_varlen_rows_equal_each_chunk_alone(cf, name, shape, chunks):
     P = int(lens.sum())
     q = randn_bf16((P, Hq, d), 17)
     eng = engine_for(cf, shape)
-    for mode in (1, 2):
+    eng.cf_set_prefill_split(1)   # cuts depend on the whole launch; these rows compare bit for bit
+    for mode in pairing_modes(shape)[1:]:
         eng.cf_set_prefill_pairing(mode)
         out = torch.full((P, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
         eng.cf_prefill_attn_varlen(q, cf.pool_of(kp, vp), lens, prefixes, table, out)

@@ -318,7 +318,8 @@ def test_layer_chunks_match_each_chunk_run_alone(cf):
     within fp32 rounding."""
     S = LayerSetup(CHUNKS_W)
     S.eng.cf_set_split_k(1)
-    for pairing in (1, 2):
+    S.eng.cf_set_prefill_split(1)   # key-range cuts depend on the whole launch
+    for pairing in (1, 2, 3):
         S.eng.cf_set_prefill_pairing(pairing)
         out = S.step().clone()
         r0 = 0
@@ -337,6 +338,7 @@ def test_layer_chunks_match_each_chunk_run_alone(cf):
         assert S.eng.cf_get_error()[0] == 0
         assert_close(od, f64(out[r0:]), "decode rows", 1e-2, 1e-3)
     S.eng.cf_set_prefill_pairing(0)
+    S.eng.cf_set_prefill_split(0)
     S.eng.cf_set_split_k(0)
 
 
