@@ -235,6 +235,8 @@ def run_cf(args, rank, world, local, pg):
     T = b.n_tokens
     eng = cf.Engine(cf.make_config(w.shape, T, max(b.n_decode, 1), args.decode_sms), W)
     eng.cf_set_graphs(args.graphs)   # piecewise CUDA graphs of the linear segments
+    eng.cf_set_prefill_pairing(args.prefill_pairing)
+    eng.cf_set_prefill_split(args.prefill_split)
     dec_ctx = torch.as_tensor(b.dec_ctx, device=dev)
     dec_pages = torch.as_tensor(b.dec_pages, device=dev)
     if len(b.chunks) > 1:   # several prefill chunks: the chunk-list form of the batch
@@ -366,7 +368,8 @@ def run_cf(args, rank, world, local, pg):
         "warmup": args.warmup, "ms_per_step": ms_step, "layer_step_us": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations and KV)",
-        "config": dict(workload_config(w, b, world), graphs=bool(args.graphs)),
+        "config": dict(workload_config(w, b, world), graphs=bool(args.graphs),
+                       prefill_pairing=args.prefill_pairing, prefill_split=args.prefill_split),
         "decode_attn_hbm_frac": (kern["decode_attn"]["gbs"] or 0) / peaks["hbm_gbs"],
         "gemm_bf16_frac": gemm_tflops / peak_tc,
         "prefill_attn_bf16_frac": (kern["prefill_attn"]["tflops"] or 0) / peak_tc,
@@ -724,6 +727,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graphs", type=int, default=0, choices=[0, 1],
                     help="replay the linear segments of the step as CUDA graphs (1) or launch eagerly (0)")
+    ap.add_argument("--prefill-pairing", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="prefill work items: 0 automatic, 1 single tiles, 2 tile pairs, 3 head pairs")
+    ap.add_argument("--prefill-split", type=int, default=0,
+                    help="prefill key-range cuts: 0 automatic, 1 never, n >= 2 n ranges")
     ap.add_argument("--kernel", choices=["decode", "prefill", "gemm", "prefill-chunks"], default=None,
                     help="run one small launch of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--estimator", default=None,

@@ -501,21 +501,50 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
     for (int i = 0; i < PER; ++i) orow[lane * PER + i] = __float2bfloat16(0.f);
     return;
   }
+  // chunk c's partial of this (request, head) sits at ((s0 + c) Hkv + h) G + g
+  const long long stride = (long long)a.Hkv * G;
+  const long long base = ((long long)s0 * a.Hkv + h) * G + g;
+  // max and sum over the chunks, the lanes taking every 32nd chunk
   float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) {
-    const long long slot = (long long)(s0 + c) * a.Hkv + h;
-    M = fmaxf(M, a.part_ml[(slot * G + g) * 2]);
-  }
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.part_ml[(base + c * stride) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   const float Mu = M == -INFINITY ? 0.f : M;
   float L = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const long long slot = (long long)(s0 + c) * a.Hkv + h;
-    const float* ml = a.part_ml + (slot * G + g) * 2;
-    const float wgt = fast_exp2(ml[0] - Mu);
-    L += wgt * ml[1];
-    const float* po = a.part_o + (slot * G + g) * D + lane * PER;
+  for (int c = lane; c < nch; c += 32) {
+    const float* ml = a.part_ml + (base + c * stride) * 2;
+    L = fmaf(fast_exp2(ml[0] - Mu), ml[1], L);
+  }
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] += wgt * po[i];
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  // O: the chunks in order (the sum order does not depend on the lanes),
+  // eight chunks' loads in flight
+  int c = 0;
+  for (; c + 8 <= nch; c += 8) {
+    float wgt[8], po[8][PER];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      wgt[u] = a.part_ml[(base + (c + u) * stride) * 2];
+      const float* src = a.part_o + (base + (c + u) * stride) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        po[u][0] = v.x; po[u][1] = v.y; po[u][2] = v.z; po[u][3] = v.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) po[u][i] = src[i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = fast_exp2(wgt[u] - Mu);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, po[u][i], acc[i]);
+    }
+  }
+  for (; c < nch; ++c) {
+    const float w = fast_exp2(a.part_ml[(base + c * stride) * 2] - Mu);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, a.part_o[(base + c * stride) * D + lane * PER + i], acc[i]);
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
 #pragma unroll

@@ -562,14 +562,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// One CTA per query tile of a cut unit, one thread per query row: the
-// partials of the unit's key ranges, each (O_s, m_s, l_s) with
-// O_s = sum exp2(s - m_s) v, combine as
+// One CTA per (query tile of a cut unit, 8 output columns), one thread per
+// query row: the partials of the unit's key ranges, each (O_s, m_s, l_s)
+// with O_s = sum exp2(s - m_s) v, combine as
 // O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M = max m_s,
-// in split order (deterministic).
+// in split order (deterministic).  Partials are column-major [D][128], so
+// each warp load is 128 consecutive bytes; four ranges' loads are issued
+// together.
+constexpr int kMergeCols = 8;
 template <int D>
 __global__ void __launch_bounds__(BQ) prefill_merge_kernel(const __grid_constant__ PrefillArgs a) {
-  const int b = blockIdx.x, r = threadIdx.x;
+  constexpr int NG = D / kMergeCols;
+  const int b = blockIdx.x / NG, cg = blockIdx.x % NG, r = threadIdx.x;
   int sl = 0;
   while (sl + 1 < a.n_chunks && a.merge_end[sl] <= b) ++sl;
   const int local = b - (sl ? a.merge_end[sl - 1] : 0);
@@ -583,38 +587,43 @@ __global__ void __launch_bounds__(BQ) prefill_merge_kernel(const __grid_constant
   if (qi >= it.len) return;
   const int S = a.splits[sl];
   const int P0 = a.part_base[sl] + 2 * u * S + x;   // split s at P0 + 2 s
-  float w[kPfMaxSplits];
-  float M = -INFINITY, L = 0.f;
-  for (int sp = 0; sp < S; ++sp) {
-    const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[(size_t)(P0 + 2 * sp) * BQ + r];
-    w[sp] = ml.y > 0.f ? ml.x : -INFINITY;
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  const float2* mlp = reinterpret_cast<const float2*>(a.part_ml) + (size_t)P0 * BQ + r;
+  float2 ml[kPfMaxSplits];
+  float M = -INFINITY;
+#pragma unroll
+  for (int sp = 0; sp < kPfMaxSplits; ++sp) {
+    ml[sp] = sp < S ? mlp[(size_t)2 * sp * BQ] : make_float2(-INFINITY, 0.f);
+    if (ml[sp].y > 0.f) M = fmaxf(M, ml[sp].x);
   }
-  for (int sp = 0; sp < S; ++sp) {
-    const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[(size_t)(P0 + 2 * sp) * BQ + r];
-    w[sp] = w[sp] == -INFINITY ? 0.f : fast_exp2(w[sp] - M);
-    L += w[sp] * ml.y;
+  float L = 0.f, o[kMergeCols];
+#pragma unroll
+  for (int i = 0; i < kMergeCols; ++i) o[i] = 0.f;
+#pragma unroll
+  for (int s4 = 0; s4 < kPfMaxSplits; s4 += 4) {
+    if (s4 >= S) break;
+    float v[4][kMergeCols], w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int sp = s4 + t;
+      // an empty range (l = 0) was never written: weight 0, nothing read
+      const bool use = sp < S && ml[sp].y > 0.f;
+      w[t] = use ? fast_exp2(ml[sp].x - M) : 0.f;
+      const float* po = a.part_o + ((size_t)(P0 + 2 * sp) * D + cg * kMergeCols) * BQ + r;
+#pragma unroll
+      for (int i = 0; i < kMergeCols; ++i) v[t][i] = use ? po[(size_t)i * BQ] : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      L = fmaf(w[t], ml[s4 + t < kPfMaxSplits ? s4 + t : 0].y, L);
+#pragma unroll
+      for (int i = 0; i < kMergeCols; ++i) o[i] = fmaf(w[t], v[t][i], o[i]);
+    }
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
-  __nv_bfloat16* orow = a.out + (size_t)(it.row0 + qi) * a.out_stride + (size_t)(x ? it.hb : it.ha) * D;
-#pragma unroll 1
-  for (int c = 0; c < D; c += 8) {
-    float o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = 0.f;
-    for (int sp = 0; sp < S; ++sp) {
-      if (w[sp] == 0.f) continue;
-      const float* po = a.part_o + (size_t)(P0 + 2 * sp) * D * BQ + r;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = fmaf(w[sp], po[(size_t)(c + i) * BQ], o[i]);
-    }
-    uint4 v;
-    v.x = pack_bf16(o[0] * inv, o[1] * inv);
-    v.y = pack_bf16(o[2] * inv, o[3] * inv);
-    v.z = pack_bf16(o[4] * inv, o[5] * inv);
-    v.w = pack_bf16(o[6] * inv, o[7] * inv);
-    *reinterpret_cast<uint4*>(orow + c) = v;
-  }
+  __nv_bfloat16* orow =
+      a.out + (size_t)(it.row0 + qi) * a.out_stride + (size_t)(x ? it.hb : it.ha) * D + cg * kMergeCols;
+  *reinterpret_cast<uint4*>(orow) = make_uint4(pack_bf16(o[0] * inv, o[1] * inv), pack_bf16(o[2] * inv, o[3] * inv),
+                                               pack_bf16(o[4] * inv, o[5] * inv), pack_bf16(o[6] * inv, o[7] * inv));
 }
 
 template <int D>
@@ -726,9 +735,9 @@ cudaError_t launch_prefill_merge(const PrefillArgs& a, cudaStream_t s) {
   const int blocks = prefill_merge_blocks(a);
   if (blocks <= 0) return cudaSuccess;
   if (a.head_dim == 128)
-    prefill_merge_kernel<128><<<blocks, BQ, 0, s>>>(a);
+    prefill_merge_kernel<128><<<blocks * (128 / kMergeCols), BQ, 0, s>>>(a);
   else if (a.head_dim == 64)
-    prefill_merge_kernel<64><<<blocks, BQ, 0, s>>>(a);
+    prefill_merge_kernel<64><<<blocks * (64 / kMergeCols), BQ, 0, s>>>(a);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
