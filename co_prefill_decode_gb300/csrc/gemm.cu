@@ -83,6 +83,18 @@ struct UnitIter {
 };
 
 CF_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// barrier of the 128 epilogue threads that also ANDs a flag over them, so a
+// wait that ran out in one warp makes all four leave together (the fix-up's
+// barriers then never wait for a warp that has left)
+CF_DEV bool epi_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 // Split-K fix-up of a tail unit (a k-chunk of a cut tile).  Returns 1 when
 // this CTA holds the tile's full sum in TMEM and must run the epilogue, 0
@@ -187,7 +199,7 @@ CF_DEV int sk_fixup(uint32_t taddr, int r_in_tile, int ep_tid, const Unit& u, co
         tmem_st32(taddr + (c0 + c) * 32, v);
       }
     }
-    epi_bar();   // the ring is read before the next round overwrites it
+    ok = epi_bar_and(ok);   // the ring is read before the next round overwrites it
   }
   tmem_st_wait();
   if (ep_tid == 0) *flag = 0;   // free for the next launch
@@ -453,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; ui.next(u); ++it) {
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
+      if (!epi_bar_and(mbar_wait(&tfull[acc], acc_phase, wc))) break;
       tc_fence_after();
       const int mt = u.tile % num_m, nt = u.tile / num_m;
       const int row = mt * BM + r_in_tile;
