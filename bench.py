@@ -237,6 +237,7 @@ def run_cf(args, rank, world, local, pg):
     eng.cf_set_graphs(args.graphs)   # piecewise CUDA graphs of the linear segments
     eng.cf_set_prefill_pairing(args.prefill_pairing)
     eng.cf_set_prefill_split(args.prefill_split)
+    eng.cf_set_split_k(args.split_k)
     dec_ctx = torch.as_tensor(b.dec_ctx, device=dev)
     dec_pages = torch.as_tensor(b.dec_pages, device=dev)
     if len(b.chunks) > 1:   # several prefill chunks: the chunk-list form of the batch
@@ -369,7 +370,8 @@ def run_cf(args, rank, world, local, pg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations and KV)",
         "config": dict(workload_config(w, b, world), graphs=bool(args.graphs),
-                       prefill_pairing=args.prefill_pairing, prefill_split=args.prefill_split),
+                       prefill_pairing=args.prefill_pairing, prefill_split=args.prefill_split,
+                       split_k=args.split_k),
         "decode_attn_hbm_frac": (kern["decode_attn"]["gbs"] or 0) / peaks["hbm_gbs"],
         "gemm_bf16_frac": gemm_tflops / peak_tc,
         "prefill_attn_bf16_frac": (kern["prefill_attn"]["tflops"] or 0) / peak_tc,
@@ -731,6 +733,8 @@ def main(argv=None):
                     help="prefill work items: 0 automatic, 1 single tiles, 2 tile pairs, 3 head pairs")
     ap.add_argument("--prefill-split", type=int, default=0,
                     help="prefill key-range cuts: 0 automatic, 1 never, n >= 2 n ranges")
+    ap.add_argument("--split-k", type=int, default=0,
+                    help="GEMM split-K tail: 0 automatic, 1 whole tiles only, n >= 2 n k-chunks")
     ap.add_argument("--kernel", choices=["decode", "prefill", "gemm", "prefill-chunks"], default=None,
                     help="run one small launch of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--estimator", default=None,

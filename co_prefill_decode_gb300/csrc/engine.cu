@@ -335,6 +335,7 @@ cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const StepChunks& ch, cons
   pa.H = c.hidden;
   pa.xn = x ? e->xn : nullptr;
   pa.rope_cs = e->rope_cs;
+  pa.cs_ld = c.max_tokens;
   pa.inv_freq = e->inv_freq;
   pa.half_dim = c.head_dim / 2;
   pa.slot = e->slot;
@@ -368,6 +369,7 @@ cf_status qkv_stage(cf_engine* e, const cf_batch* bt, const StepChunks& ch, cons
   g.qkv.num_pages = pool->num_pages;
   g.qkv.eps = c.rms_eps;
   g.qkv.rope_cs = e->rope_cs;
+  g.qkv.cs_ld = c.max_tokens;
   g.qkv.slot = e->slot;
   g.qkv.g_q = static_cast<const __nv_bfloat16*>(e->w.g_q);
   g.qkv.g_k = static_cast<const __nv_bfloat16*>(e->w.g_k);

@@ -262,7 +262,8 @@ CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpi
     }
     nrm = rsqrtf(ss / D + e.eps);
   }
-  const float2* cs = e.rope_cs + (size_t)(valid ? row : 0) * (D / 2);
+  // pair-major table: for pair i the warp's 32 rows are 256 contiguous bytes
+  const float2* cs = e.rope_cs + (valid ? row : 0);
   // rotate-half: element i pairs with i + D/2
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
@@ -278,7 +279,7 @@ CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpi
         x1 *= bf16f(g[i0]);
         x2 *= bf16f(g[i0 + D / 2]);
       }
-      const float2 r = cs[i0];
+      const float2 r = cs[(size_t)i0 * e.cs_ld];
       v[i] = x1 * r.x - x2 * r.y;
       w[i] = x1 * r.y + x2 * r.x;
     }

@@ -40,7 +40,8 @@ enum GemmEpi {
 struct QkvEpilogue {
   int Hq, Hkv, head_dim, page_size, qk_norm, num_pages;
   float eps;
-  const float2* rope_cs;          // [T][d/2] (cos, sin) at each row's position
+  const float2* rope_cs;          // [d/2][cs_ld] (cos, sin) at each row's position, pair-major
+  int cs_ld;                      // row stride of rope_cs (>= T)
   const int* slot;                // [T] pool slot of each row (-1: skip)
   const __nv_bfloat16* g_q;       // [d]
   const __nv_bfloat16* g_k;       // [d]
@@ -117,7 +118,8 @@ struct PrepArgs {
   int T, H;
   __nv_bfloat16* xn;              // [T][H]
   // rope table + slots (skipped when rope_cs == nullptr)
-  float2* rope_cs;                // [T][d/2]
+  float2* rope_cs;                // [d/2][cs_ld]: pair-major, so a warp's rows read 256 contiguous bytes
+  int cs_ld;
   const double* inv_freq;         // [d/2]
   int half_dim;
   int* slot;                      // [T]

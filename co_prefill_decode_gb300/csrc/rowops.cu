@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
     const double r = ang - rint(ang / two_pi) * two_pi;
     float s, c;
     sincosf((float)r, &s, &c);
-    a.rope_cs[(size_t)row * a.half_dim + i] = make_float2(c, s);
+    a.rope_cs[(size_t)i * a.cs_ld + row] = make_float2(c, s);
   }
 }
 
