@@ -492,19 +492,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid) store_bf16x32(out + c, v);
         }
       } else if constexpr (EPI == EPI_RESID_F32) {
+        // the residual of chunk c + 32 is loaded while chunk c is read from
+        // TMEM and stored, so only the first chunk waits for its loads
         float* out = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + nt * BN;
-        const __nv_bfloat16* res =
-            reinterpret_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * p.ld_aux + nt * BN;
+        const uint4* res = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.aux) +
+                                                          (size_t)row * p.ld_aux + nt * BN);
+        uint4 rn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rn[i] = valid ? res[i] : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
+          uint4 rc[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rc[i] = rn[i];
+          if (valid && c + 32 < BN) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rn[i] = res[(c + 32) / 8 + i];
+          }
           tmem_ld32(taddr + c, v);
           tmem_ld_wait();
           if (valid) {
-            const uint4* r4 = reinterpret_cast<const uint4*>(res + c);
             float4* o4 = reinterpret_cast<float4*>(out + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint4 q = r4[i];
+              const uint4 q = rc[i];
               o4[2 * i] = make_float4(v[8 * i + 0] + bf16lo(q.x), v[8 * i + 1] + bf16hi(q.x),
                                       v[8 * i + 2] + bf16lo(q.y), v[8 * i + 3] + bf16hi(q.y));
               o4[2 * i + 1] = make_float4(v[8 * i + 4] + bf16lo(q.z), v[8 * i + 5] + bf16hi(q.z),
