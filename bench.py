@@ -36,7 +36,7 @@ METRIC = "co-batched layer step µs & tokens/s; decode attn % HBM peak; GEMM % B
 # DRAM bytes (read + write) per launch of the roofline kernel, from one ncu
 # capture of the same kernel build; cleared whenever that kernel changes.
 DOMINANT_TRAFFIC = {
-    "l8b": {"bytes": 243602944 + 22031872, "source": "profiles/gemm_gateup_l8b_T1040.md"},
+    "l8b": {"bytes": 243638528 + 22196480, "source": "profiles/gemm_gateup_l8b_T1040.md"},
 }
 
 
