@@ -347,7 +347,8 @@ def run_cf(args, rank, world, local, pg):
                            "sms": eng.cf_engine_decode_sms()}
     kern["prefill_attn"] = {"ms": per["prefill"],
                             "tflops": wk["prefill_flops"] / t_pre / 1e12 if t_pre > 0 else None}
-    kern["fork"] = {"ms": per["fork"], "serial_ms": per["decode"] + per["prefill"]}
+    kern["fork"] = {"ms": per["fork"], "serial_ms": per["decode"] + per["prefill"],
+                    "to_decode_start_ms": per.get("fork_in"), "decode_end_to_join_ms": per.get("fork_out")}
     kern["rmsnorm"] = {"ms": per["rmsnorm"] + per["rmsnorm2"]}
     gemm_ms = sum(per[k] for k in ("qkv", "oproj", "gateup", "down"))
     gemm_tflops = sum(wk["gemm_flops"].values()) / (gemm_ms / 1e3) / 1e12

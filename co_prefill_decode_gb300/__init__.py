@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_PKG, "libcf.so")
 
 CF_OK, CF_ERR_INVALID_ARG, CF_ERR_UNSUPPORTED, CF_ERR_CUDA, CF_ERR_TIMEOUT, CF_ERR_OOM, CF_ERR_DEVICE = range(7)
 CF_EPI_NONE, CF_EPI_RESID_F32, CF_EPI_RESID_BF16, CF_EPI_SWIGLU = range(4)
-PHASES = ("rmsnorm", "qkv", "decode", "prefill", "fork", "oproj", "rmsnorm2", "gateup", "down", "step")
+PHASES = ("rmsnorm", "qkv", "decode", "prefill", "fork", "oproj", "rmsnorm2", "gateup", "down", "step",
+          "fork_in", "fork_out")
 
 # every symbol include/cf.h declares
 EXPORTS = (

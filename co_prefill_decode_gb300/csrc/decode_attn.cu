@@ -41,7 +41,7 @@ constexpr int kBarBytes = 1024;                      // per-slot mbarriers
 // + 1 KB so the base can be aligned to 1 KB by hand; > half an SM, so a decode
 // CTA never shares an SM with a prefill CTA
 constexpr int kDecodeSmem = kPlanBytes + kRingBytes + kBarBytes + 1024;
-constexpr int kItemsPerWarp = 4;
+constexpr int kItemsPerWarp = 4;   // items per warp the plan aims at (unequal lengths)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: O is rescaled only when the max grows more
 
 template <int D>
@@ -244,8 +244,11 @@ CF_DEV void write_row(const float (*o)[2], float m, float l, bool final_out, __n
 
 // Chunking plan, computed identically by every CTA of every grid from the
 // key counts: pages_j = ceil(keys_j / 16); chunk = max(4, ceil(sum_j pages_j
-// * Hkv / (4 * warps))) with warps = 8 * plan_ctas; chunks_j =
-// ceil(pages_j / chunk); S_j = prefix sums.
+// * Hkv / (ipw * warps))) with warps = 8 * plan_ctas; chunks_j =
+// ceil(pages_j / chunk); S_j = prefix sums.  ipw = 4 items per warp, or 2
+// when every request has about the same length (longest <= 1.25 x mean):
+// equal requests give equal items, so the queue stays balanced with fewer,
+// longer items, which start up fewer times and leave fewer partials to merge.
 CF_DEV int build_plan(const DecodeArgs& a, int* s_pref, int* s_pages) {
   const int n = a.n;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
@@ -263,11 +266,19 @@ CF_DEV int build_plan(const DecodeArgs& a, int* s_pref, int* s_pages) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     long long tot = 0;
-    for (int j = lane; j < n; j += 32) tot += s_pages[j];
+    int pmax = 0;
+    for (int j = lane; j < n; j += 32) {
+      tot += s_pages[j];
+      pmax = max(pmax, s_pages[j]);
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
+    }
     const long long warps = (long long)a.plan_ctas * kDecodeWarps;
-    long long chunk = (tot * a.Hkv + kItemsPerWarp * warps - 1) / (kItemsPerWarp * warps);
+    const long long ipw = 4LL * pmax * n <= 5LL * tot ? kItemsPerWarp / 2 : kItemsPerWarp;
+    long long chunk = (tot * a.Hkv + ipw * warps - 1) / (ipw * warps);
     if (chunk < 4) chunk = 4;
     // exclusive prefix sum of chunks_j: lane owns a contiguous block of j
     const int per = (n + 31) / 32;
@@ -504,27 +515,33 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
   // chunk c's partial of this (request, head) sits at ((s0 + c) Hkv + h) G + g
   const long long stride = (long long)a.Hkv * G;
   const long long base = ((long long)s0 * a.Hkv + h) * G + g;
-  // max and sum over the chunks, the lanes taking every 32nd chunk
-  float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.part_ml[(base + c * stride) * 2]);
+  const float2* mlp = reinterpret_cast<const float2*>(a.part_ml);
+  // (m, l) of chunks lane and lane + 32 stay in registers; later chunks
+  // (more than 64, rare) are read again in the O pass
+  const float2 ninf = make_float2(-INFINITY, 0.f);
+  const float2 ml0 = lane < nch ? mlp[base + lane * stride] : ninf;
+  const float2 ml1 = lane + 32 < nch ? mlp[base + (lane + 32) * stride] : ninf;
+  float M = fmaxf(ml0.x, ml1.x);
+  for (int c = lane + 64; c < nch; c += 32) M = fmaxf(M, mlp[base + c * stride].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   const float Mu = M == -INFINITY ? 0.f : M;
-  float L = 0.f;
-  for (int c = lane; c < nch; c += 32) {
-    const float* ml = a.part_ml + (base + c * stride) * 2;
-    L = fmaf(fast_exp2(ml[0] - Mu), ml[1], L);
+  const float w0 = fast_exp2(ml0.x - Mu), w1 = fast_exp2(ml1.x - Mu);   // exp2(-inf) = 0
+  float L = fmaf(w0, ml0.y, w1 * ml1.y);
+  for (int c = lane + 64; c < nch; c += 32) {
+    const float2 ml = mlp[base + c * stride];
+    L = fmaf(fast_exp2(ml.x - Mu), ml.y, L);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   // O: the chunks in order (the sum order does not depend on the lanes),
-  // eight chunks' loads in flight
+  // sixteen chunks' loads in flight; chunk c's weight comes from lane c % 32
+  constexpr int B = 16;
   int c = 0;
-  for (; c + 8 <= nch; c += 8) {
-    float wgt[8], po[8][PER];
+  for (; c + B <= nch; c += B) {
+    float po[B][PER];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      wgt[u] = a.part_ml[(base + (c + u) * stride) * 2];
+    for (int u = 0; u < B; ++u) {
       const float* src = a.part_o + (base + (c + u) * stride) * D + lane * PER;
       if constexpr (PER == 4) {
         const float4 v = *reinterpret_cast<const float4*>(src);
@@ -535,14 +552,17 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
       }
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float w = fast_exp2(wgt[u] - Mu);
+    for (int u = 0; u < B; ++u) {
+      const int cu = c + u;
+      const float wa = __shfl_sync(0xffffffffu, w0, cu & 31), wb = __shfl_sync(0xffffffffu, w1, cu & 31);
+      const float w = cu < 32 ? wa : (cu < 64 ? wb : fast_exp2(mlp[base + cu * stride].x - Mu));
 #pragma unroll
       for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, po[u][i], acc[i]);
     }
   }
   for (; c < nch; ++c) {
-    const float w = fast_exp2(a.part_ml[(base + c * stride) * 2] - Mu);
+    const float wa = __shfl_sync(0xffffffffu, w0, c & 31), wb = __shfl_sync(0xffffffffu, w1, c & 31);
+    const float w = c < 32 ? wa : (c < 64 ? wb : fast_exp2(mlp[base + c * stride].x - Mu));
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, a.part_o[(base + c * stride) * D + lane * PER + i], acc[i]);
   }

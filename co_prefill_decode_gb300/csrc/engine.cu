@@ -85,9 +85,10 @@ using namespace cf;
 namespace {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s cap on any one device wait
-constexpr int kPhases = 10;
+constexpr int kPhases = 12;
 constexpr int kRing = 64;
-enum { PH_PREP = 0, PH_QKV, PH_DEC, PH_PRE, PH_FORK, PH_OPROJ, PH_PREP2, PH_GU, PH_DOWN, PH_STEP };
+enum { PH_PREP = 0, PH_QKV, PH_DEC, PH_PRE, PH_FORK, PH_OPROJ, PH_PREP2, PH_GU, PH_DOWN, PH_STEP, PH_FORK_IN,
+       PH_FORK_OUT };
 enum { EV_START = 0, EV_PREP, EV_QKV, EV_DEC0, EV_DEC1, EV_PRE0, EV_PRE1, EV_JOIN, EV_OPROJ, EV_PREP2, EV_GU, EV_END,
        EV_COUNT };
 
@@ -410,7 +411,11 @@ void prof_resolve(cf_engine* e, int slot) {
   };
   e->phase_ms[PH_PREP] += el(EV_START, EV_PREP);
   e->phase_ms[PH_QKV] += el(EV_PREP, EV_QKV);
-  if (e->ring_has_dec[slot]) e->phase_ms[PH_DEC] += el(EV_DEC0, EV_DEC1);
+  if (e->ring_has_dec[slot]) {
+    e->phase_ms[PH_DEC] += el(EV_DEC0, EV_DEC1);
+    e->phase_ms[PH_FORK_IN] += el(EV_QKV, EV_DEC0);
+    e->phase_ms[PH_FORK_OUT] += el(EV_DEC1, EV_JOIN);
+  }
   if (e->ring_has_pre[slot]) e->phase_ms[PH_PRE] += el(EV_PRE0, EV_PRE1);
   e->phase_ms[PH_FORK] += el(EV_QKV, EV_JOIN);
   e->phase_ms[PH_OPROJ] += el(EV_JOIN, EV_OPROJ);

@@ -346,7 +346,9 @@ cf_status cf_get_error(cf_engine* e, char* buf, int len);
  * cf_set_profiling: 1 = record CUDA events around every phase of each step.
  * cf_get_phase_times: accumulated milliseconds per phase since the last
  *   reset (order: rmsnorm, qkv, decode, prefill, fork, oproj, rmsnorm2,
- *   gateup, down, step) and the number of steps; resets the counters.
+ *   gateup, down, step, fork_in = fork start to the decode grid's start,
+ *   fork_out = the decode grid's end to the join) and the number of steps;
+ *   resets the counters.
  * cf_launch_count: kernels this engine launched since creation. */
 void* cf_engine_buffer(cf_engine* e, const char* name);
 int cf_engine_decode_sms(cf_engine* e);
