@@ -188,7 +188,7 @@ cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t s);
 // that read the same KV head (GQA groups of even size).
 constexpr int kPfSingle = 0, kPfTilePairs = 1, kPfHeadPairs = 2;
 constexpr int kPfMaxSplits = 16;
-constexpr int kPfPartTiles = 512;   // fp32 partial (query tile) slots of split items per engine
+constexpr int kPfPartTiles = 2048;  // fp32 partial (query tile) slots of split items per engine (128 MB at d = 128)
 
 struct PrefillArgs {
   // Work items are numbered chunk slot by chunk slot (slots sorted so that the

@@ -689,6 +689,12 @@ void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix
   }
   const double avg = (double)total / (sms > 0 ? sms : 1);
   const double target = avg > 8.0 ? avg : 8.0;   // shortest range worth a split of its own
+  // Few long units for the grid (fewer than 4 per SM) leave the last wave
+  // part-empty: cut them so there are about 4 per SM, at most 4 ranges of at
+  // least 16 key tiles each (q14b's 320 pair units on 152 SMs: cut in 2).
+  int all_units = 0;
+  for (int i = 0; i < n; ++i) all_units += units[i];
+  const int quant = all_units > 0 && all_units < 4 * sms ? std::min(4, (4 * sms + all_units - 1) / all_units) : 1;
   a.n_chunks = n;
   int items = 0, parts = 0, merges = 0;
   for (int s = 0; s < n; ++s) {
@@ -696,8 +702,10 @@ void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix
     int S = 1;
     if (split_mode >= 2)
       S = split_mode;
-    else if (split_mode == 0 && reach_max[i] > 1.25 * target)
-      S = (int)std::ceil(reach_max[i] / target);
+    else if (split_mode == 0) {
+      if (reach_max[i] > 1.25 * target) S = (int)std::ceil(reach_max[i] / target);
+      S = std::max(S, std::min(quant, reach_min[i] / 16));
+    }
     S = std::min(S, std::min(reach_min[i], kPfMaxSplits));   // every split has a key tile
     if (S > 1 && parts + 2 * units[i] * S > kPfPartTiles) S = (kPfPartTiles - parts) / (2 * units[i]);
     if (S < 2) S = 1;
