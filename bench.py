@@ -9,7 +9,9 @@ paged append, the decode || prefill attention fork, O-proj, RMSNorm, SwiGLU
 FFN).  `value` is stacked tokens per second (T rows per step) with inputs
 resident in HBM; `e2e` times the same step through host (pinned) buffers
 with the per-step host->device copies of x and of the batch metadata and the
-device->host copy of the output inside the timed region.  N > 1 runs N
+device->host copy of the output inside the timed region (on their own
+streams, double-buffered: a step's copies overlap its neighbours' compute,
+as a serving loop would run them).  N > 1 runs N
 independent replicas (one per GPU, no collective in the data path) and
 reports the total over ranks divided by the slowest rank's time.
 
@@ -300,32 +302,64 @@ def run_cf(args, rank, world, local, pg):
     phases, nsteps = eng.cf_get_phase_times()
     eng.cf_set_profiling(False)
 
-    # e2e: host buffers, copies inside the timed region
+    # e2e: host buffers, copies inside the timed region.  Every step copies its
+    # input rows and batch metadata from pinned host memory and reads its output
+    # back; the copies run on their own streams, double-buffered, so step i's
+    # input copy overlaps step i-1 and its output read overlaps step i+1.
     x_host = x.cpu().pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
-    meta_host = [t.cpu().pin_memory() for t in (dec_ctx, dec_pages, pre_pages)]
-    meta_dev = (dec_ctx, dec_pages, pre_pages)
+    meta_dev0 = (dec_ctx, dec_pages, pre_pages)
+    meta_host = [t.cpu().pin_memory() for t in meta_dev0]
+    xs = [x, torch.empty_like(x)]
+    outs = [out, torch.empty_like(out)]
+    out_hosts = [torch.empty(x_host.shape, dtype=x_host.dtype).pin_memory() for _ in range(2)]
+    metas = [meta_dev0, tuple(torch.empty_like(t) for t in meta_dev0)]
+    if len(b.chunks) > 1:
+        batches = [cf.batch_of(b.n_decode, m[0], m[1], 0, 0, None, chunks=(lens, prefixes, m[2])) for m in metas]
+    else:
+        batches = [cf.batch_of(b.n_decode, m[0], m[1], b.prefill_len, b.prefill_prefix, m[2]) for m in metas]
     h2d = x_host.numel() * 2 + sum(t.numel() * 4 for t in meta_host)
-    d2h = out_host.numel() * 2
+    d2h = out_hosts[0].numel() * 2
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def e2e_step():
-        x.copy_(x_host, non_blocking=True)
-        for hsrc, ddst in zip(meta_host, meta_dev):
-            ddst.copy_(hsrc, non_blocking=True)
-        eng.cf_layer_step(batch, x, out, pool, stream)
-        out_host.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            if used[k]:
+                s_in.wait_event(ev_done[k])   # step i-2 has finished with these buffers
+            xs[k].copy_(x_host, non_blocking=True)
+            for hsrc, ddst in zip(meta_host, metas[k]):
+                ddst.copy_(hsrc, non_blocking=True)
+            ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        if used[k]:
+            stream.wait_event(ev_read[k])     # step i-2's output has been read back
+        eng.cf_layer_step(batches[k], xs[k], outs[k], pool, stream)
+        ev_done[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[k])
+            out_hosts[k].copy_(outs[k], non_blocking=True)
+            ev_read[k].record(s_out)
+        used[k] = True
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(pg)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    for i in range(args.steps):
+        e2e_step(i)
+    for k in range(2):
+        stream.wait_event(ev_read[k])         # the last outputs are back on the host
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(pg)
+    e2e_ok = bool(torch.equal(out_hosts[(args.steps - 1) % 2], out.cpu()))   # the read-back is the step's output
     ms_e2e = max_over_ranks(pg, e0.elapsed_time(e1), dev)
     st, msg = eng.cf_get_error()
     if st != 0:
@@ -382,7 +416,7 @@ def run_cf(args, rank, world, local, pg):
         "decode_sms_calibration": calib,
         "roofline": roofline,
         "e2e": {"value": tok_total / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "copies": "own streams, double-buffered", "output_read_back_ok": e2e_ok},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "peaks": peaks,
