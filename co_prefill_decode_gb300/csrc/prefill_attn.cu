@@ -163,6 +163,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch();
   if (!a.pdl) griddep_wait();
+  if (a.pdl) {
+    // A grid joining a running queue (the fork's second prefill grid): if
+    // every item has been taken already, leave before any set-up.  The
+    // counter only grows, so a stale read just means no early exit.
+    __shared__ int s_drained;
+    if (threadIdx.x == 0)
+      s_drained = *reinterpret_cast<volatile unsigned*>(a.counter) - a.base >= (unsigned)a.item_end[a.n_chunks - 1];
+    __syncthreads();
+    if (s_drained) return;
+  }
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);

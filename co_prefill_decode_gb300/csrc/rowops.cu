@@ -118,10 +118,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
     a.slot[row] = slot;
   }
   // angle = pos * theta^(-2i/d) in double, reduced modulo 2*pi, then sincos
+  // (the nearest multiple of 2 pi is found with a multiply by 1 / (2 pi):
+  // FP64 division is slow here, and a quotient off by one only moves r by
+  // 2 pi, which sincos does not see)
   const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
   for (int i = threadIdx.x; i < a.half_dim; i += kPrepThreads) {
     const double ang = (double)pos * a.inv_freq[i];
-    const double r = ang - rint(ang / two_pi) * two_pi;
+    const double r = ang - rint(ang * inv_two_pi) * two_pi;
     float s, c;
     sincosf((float)r, &s, &c);
     a.rope_cs[(size_t)i * a.cs_ld + row] = make_float2(c, s);
