@@ -29,7 +29,7 @@ EXPORTS = (
     "cf_prefill_attn", "cf_gemm", "cf_kv_append", "cf_get_error", "cf_engine_buffer",
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
-    "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
+    "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_prefill_plan", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
     "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate", "cf_waterfill_dispatch",
     "cf_waterfill_assign", "cf_prefill_attn_varlen", "cf_set_prefill_split",
 )
@@ -129,6 +129,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_gemm_schedule": (I, [I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                                  ctypes.POINTER(I)]),
         "cf_set_split_k": (I, [P, I]),
+        "cf_prefill_plan": (I, [I, P, P, I, I, I, I, I, ctypes.POINTER(I), P, ctypes.POINTER(I)]),
         "cf_selftest_timeout": (I, [P, ctypes.c_ulonglong, P]),
         "cf_set_prefill_pairing": (I, [P, I]),
         "cf_set_prefill_split": (I, [P, I]),
@@ -188,6 +189,21 @@ def cf_gemm_schedule(M: int, N: int, K: int, epilogue: int = CF_EPI_NONE, ctas: 
     _check(lib, None, lib.cf_gemm_schedule(M, N, K, epilogue, ctas, split_mode, ctypes.byref(g),
                                            ctypes.byref(t), ctypes.byref(d), ctypes.byref(sp)))
     return {"grid": g.value, "tiles": t.value, "dp_tiles": d.value, "split": sp.value}
+
+
+def cf_prefill_plan(chunks, n_q_heads: int, n_kv_heads: int, sms: int = 152, split_mode: int = 0,
+                    pairing_mode: int = 0) -> dict:
+    """Work plan of one prefill launch over chunks [(len, prefix), ...] (host only)."""
+    lib = load_library()
+    n = len(chunks)
+    lens = (ctypes.c_int * max(n, 1))(*[int(c[0]) for c in chunks])
+    prefixes = (ctypes.c_int * max(n, 1))(*[int(c[1]) for c in chunks])
+    splits = (ctypes.c_int * max(n, 1))()
+    kind, items = ctypes.c_int(), ctypes.c_int()
+    _check(lib, None, lib.cf_prefill_plan(n, ctypes.cast(lens, ctypes.c_void_p), ctypes.cast(prefixes, ctypes.c_void_p),
+                                          n_q_heads, n_kv_heads, sms, split_mode, pairing_mode, ctypes.byref(kind),
+                                          ctypes.cast(splits, ctypes.c_void_p), ctypes.byref(items)))
+    return {"kind": kind.value, "splits": list(splits)[:n], "items": items.value}
 
 
 def make_config(shape, max_tokens: int, max_decode: int, decode_sms: int = 0, page_size: int = 16) -> cf_config:

@@ -1035,6 +1035,33 @@ cf_status cf_gemm_schedule(int M, int N, int K, int epilogue, int ctas, int spli
   return CF_OK;
 }
 
+cf_status cf_prefill_plan(int n, const int* len, const int* prefix, int n_q_heads, int n_kv_heads, int sms,
+                          int split_mode, int pairing_mode, int* kind, int* splits, int* items) {
+  if (n <= 0 || n > kMaxChunks || !len || !prefix || n_q_heads <= 0 || n_kv_heads <= 0 || sms <= 0 ||
+      n_q_heads % n_kv_heads || split_mode < 0 || split_mode > kPfMaxSplits || pairing_mode < 0 || pairing_mode > 3)
+    return CF_ERR_INVALID_ARG;
+  if (pairing_mode == 3 && (n_q_heads / n_kv_heads) % 2) return CF_ERR_UNSUPPORTED;
+  int row0[kMaxChunks], off[kMaxChunks];
+  int r = 0;
+  for (int i = 0; i < n; ++i) {
+    if (len[i] <= 0 || prefix[i] < 0) return CF_ERR_INVALID_ARG;
+    row0[i] = r;
+    off[i] = 0;
+    r += len[i];
+  }
+  PrefillArgs pf{};
+  pf.Hq = n_q_heads;
+  pf.Hkv = n_kv_heads;
+  pf.pair = pairing_mode ? pairing_mode - 1 : prefill_pairing(len, n, n_q_heads, n_kv_heads, sms);
+  prefill_set_chunks(pf, n, len, prefix, row0, off, sms, split_mode);
+  for (int s = 0; s < n; ++s)   // slots are sorted by reach: map them back to the given order
+    for (int i = 0; i < n; ++i)
+      if (row0[i] == pf.row0[s] && splits) splits[i] = pf.splits[s];
+  if (kind) *kind = pf.pair;
+  if (items) *items = prefill_items(pf);
+  return CF_OK;
+}
+
 cf_status cf_set_prefill_pairing(cf_engine* e, int mode) {
   if (!e || mode < 0 || mode > 3) return CF_ERR_INVALID_ARG;
   if (mode == 3 && (e->cfg.n_q_heads / e->cfg.n_kv_heads) % 2) return fail(e, CF_ERR_UNSUPPORTED, "odd GQA group");

@@ -135,6 +135,20 @@ cf_status cf_set_graphs(cf_engine* e, int enable);
 /* Number of graph pairs this engine has captured so far. */
 long long cf_graph_captures(cf_engine* e);
 
+/* The work plan of one prefill launch (host only; needs no GPU), as the
+ * layer step and cf_prefill_attn_varlen make it for n chunks (len[i],
+ * prefix[i]) given in stacked-row order on `sms` SMs.  *kind: the work unit,
+ * 0 single 128-row query tiles, 1 pairs of consecutive query tiles of one
+ * head, 2 pairs of query heads of one KV head on one query tile (used when
+ * Hq / Hkv is even); pairing_mode 0 chooses it as the engine does, 1..3 force
+ * kind 0..2.  splits[i]: the key ranges each unit of chunk i is cut into
+ * (1: not cut; see cf_set_prefill_split for split_mode); *items: the queue
+ * length, sum_i units_i * splits[i].  Any output may be NULL.  Returns
+ * CF_ERR_INVALID_ARG for bad sizes, CF_ERR_UNSUPPORTED for head pairs with
+ * an odd group. */
+cf_status cf_prefill_plan(int n, const int* len, const int* prefix, int n_q_heads, int n_kv_heads, int sms,
+                          int split_mode, int pairing_mode, int* kind, int* splits, int* items);
+
 /* Work items of prefill attention.  Each item runs two 128-row query tiles
  * that share every K/V tile it loads, or one:
  *   1 single tiles;
