@@ -701,7 +701,8 @@ void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix
   const double target = avg > 8.0 ? avg : 8.0;   // shortest range worth a split of its own
   // Few long units for the grid (fewer than 4 per SM) leave the last wave
   // part-empty: cut them so there are about 4 per SM, at most 4 ranges of at
-  // least 16 key tiles each (q14b's 320 pair units on 152 SMs: cut in 2).
+  // least 16 key tiles each (a 2048-token chunk of 40 query heads: 320
+  // tile-pair units on 152 SMs, cut in 2).
   int all_units = 0;
   for (int i = 0; i < n; ++i) all_units += units[i];
   const int quant = all_units > 0 && all_units < 4 * sms ? std::min(4, (4 * sms + all_units - 1) / all_units) : 1;
