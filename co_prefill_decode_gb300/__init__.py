@@ -29,7 +29,7 @@ EXPORTS = (
     "cf_prefill_attn", "cf_gemm", "cf_kv_append", "cf_get_error", "cf_engine_buffer",
     "cf_engine_decode_sms", "cf_set_decode_sms", "cf_set_profiling", "cf_get_phase_times",
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
-    "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_prefill_plan", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
+    "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_prefill_plan", "cf_decode_plan", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
     "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate", "cf_waterfill_dispatch",
     "cf_waterfill_assign", "cf_prefill_attn_varlen", "cf_set_prefill_split",
 )
@@ -130,6 +130,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                  ctypes.POINTER(I)]),
         "cf_set_split_k": (I, [P, I]),
         "cf_prefill_plan": (I, [I, P, P, I, I, I, I, I, ctypes.POINTER(I), P, ctypes.POINTER(I)]),
+        "cf_decode_plan": (I, [I, P, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(L)]),
         "cf_selftest_timeout": (I, [P, ctypes.c_ulonglong, P]),
         "cf_set_prefill_pairing": (I, [P, I]),
         "cf_set_prefill_split": (I, [P, I]),
@@ -204,6 +205,17 @@ def cf_prefill_plan(chunks, n_q_heads: int, n_kv_heads: int, sms: int = 152, spl
                                           n_q_heads, n_kv_heads, sms, split_mode, pairing_mode, ctypes.byref(kind),
                                           ctypes.cast(splits, ctypes.c_void_p), ctypes.byref(items)))
     return {"kind": kind.value, "splits": list(splits)[:n], "items": items.value}
+
+
+def cf_decode_plan(n_keys, page_stride: int, n_kv_heads: int, plan_ctas: int = 152) -> dict:
+    """Work plan of one decode launch over requests with n_keys keys each (host only)."""
+    lib = load_library()
+    n = len(n_keys)
+    keys = (ctypes.c_int * max(n, 1))(*[int(k) for k in n_keys])
+    chunk, items, mx = ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
+    _check(lib, None, lib.cf_decode_plan(n, ctypes.cast(keys, ctypes.c_void_p), page_stride, n_kv_heads, plan_ctas,
+                                         ctypes.byref(chunk), ctypes.byref(items), ctypes.byref(mx)))
+    return {"chunk": chunk.value, "items": items.value, "max_items": mx.value}
 
 
 def make_config(shape, max_tokens: int, max_decode: int, decode_sms: int = 0, page_size: int = 16) -> cf_config:

@@ -41,7 +41,6 @@ constexpr int kBarBytes = 1024;                      // per-slot mbarriers
 // + 1 KB so the base can be aligned to 1 KB by hand; > half an SM, so a decode
 // CTA never shares an SM with a prefill CTA
 constexpr int kDecodeSmem = kPlanBytes + kRingBytes + kBarBytes + 1024;
-constexpr int kItemsPerWarp = 4;   // items per warp the plan aims at (unequal lengths)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: O is rescaled only when the max grows more
 
 template <int D>
@@ -276,10 +275,7 @@ CF_DEV int build_plan(const DecodeArgs& a, int* s_pref, int* s_pages) {
       tot += __shfl_xor_sync(0xffffffffu, tot, o);
       pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
     }
-    const long long warps = (long long)a.plan_ctas * kDecodeWarps;
-    const long long ipw = 4LL * pmax * n <= 5LL * tot ? kItemsPerWarp / 2 : kItemsPerWarp;
-    long long chunk = (tot * a.Hkv + ipw * warps - 1) / (ipw * warps);
-    if (chunk < 4) chunk = 4;
+    const long long chunk = decode_plan_chunk(tot, pmax, n, a.Hkv, a.plan_ctas);
     // exclusive prefix sum of chunks_j: lane owns a contiguous block of j
     const int per = (n + 31) / 32;
     const int j0 = lane * per, j1 = min(n, j0 + per);

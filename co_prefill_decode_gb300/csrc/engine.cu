@@ -1035,6 +1035,28 @@ cf_status cf_gemm_schedule(int M, int N, int K, int epilogue, int ctas, int spli
   return CF_OK;
 }
 
+cf_status cf_decode_plan(int n, const int* n_keys, int page_stride, int n_kv_heads, int plan_ctas, int* chunk,
+                         int* items, long long* max_items) {
+  if (n <= 0 || !n_keys || page_stride <= 0 || n_kv_heads <= 0 || plan_ctas <= 0) return CF_ERR_INVALID_ARG;
+  long long tot = 0, pmax = 0;
+  std::vector<long long> pages(n);
+  for (int j = 0; j < n; ++j) {   // as the kernel: no keys -> no pages, at most the page table's width
+    const long long keys = n_keys[j];
+    long long pg = keys > 0 ? (keys + 15) / 16 : 0;
+    if (pg > page_stride) pg = page_stride;
+    pages[j] = pg;
+    tot += pg;
+    pmax = pg > pmax ? pg : pmax;
+  }
+  const long long c = decode_plan_chunk(tot, pmax, n, n_kv_heads, plan_ctas);
+  long long it = 0;
+  for (int j = 0; j < n; ++j) it += (pages[j] + c - 1) / c;
+  if (chunk) *chunk = (int)c;
+  if (items) *items = (int)(it * n_kv_heads);
+  if (max_items) *max_items = decode_max_items(n, n_kv_heads, plan_ctas);
+  return CF_OK;
+}
+
 cf_status cf_prefill_plan(int n, const int* len, const int* prefix, int n_q_heads, int n_kv_heads, int sms,
                           int split_mode, int pairing_mode, int* kind, int* splits, int* items) {
   if (n <= 0 || n > kMaxChunks || !len || !prefix || n_q_heads <= 0 || n_kv_heads <= 0 || sms <= 0 ||

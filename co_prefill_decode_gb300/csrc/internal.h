@@ -171,6 +171,18 @@ struct DecodeArgs {
   unsigned long long wait_ns;     // cap of one mbarrier wait
 };
 constexpr int kDecodeWarps = 8;
+constexpr int kItemsPerWarp = 4;   // decode items per warp the plan aims at (unequal lengths)
+// Pages per decode item (the chunk), from the total and the longest page
+// count of the n requests and the CTAs the plan is sized for: about
+// kItemsPerWarp items per warp, or half as many when every request has about
+// the same length (longest <= 1.25 x mean), at least 4 pages.
+__host__ __device__ inline long long decode_plan_chunk(long long tot_pages, long long max_pages, int n, int Hkv,
+                                                       int plan_ctas) {
+  const long long warps = (long long)plan_ctas * kDecodeWarps;
+  const long long ipw = 4LL * max_pages * n <= 5LL * tot_pages ? kItemsPerWarp / 2 : kItemsPerWarp;
+  const long long chunk = (tot_pages * Hkv + ipw * warps - 1) / (ipw * warps);
+  return chunk < 4 ? 4 : chunk;
+}
 long long decode_max_items(int max_decode, int Hkv, int max_ctas);
 // tmK/tmV: 2-D {d, pages*Hkv*ps} maps over the pools, box {64, 16}, 128-byte swizzle.
 // launch_decode = launch_decode_kernel + launch_decode_merge.  Several

@@ -135,6 +135,16 @@ cf_status cf_set_graphs(cf_engine* e, int enable);
 /* Number of graph pairs this engine has captured so far. */
 long long cf_graph_captures(cf_engine* e);
 
+/* The work plan of one decode launch (host only; needs no GPU), as the
+ * decode kernels compute it on the device from the key counts n_keys[j]
+ * (page table width page_stride pages) for a plan sized to plan_ctas CTAs:
+ * each request's pages are cut into chunks of *chunk pages, one work item
+ * per (request, KV head, chunk); *items is their count and *max_items the
+ * bound the engine's partial-output workspace is sized for (n decodes on
+ * plan_ctas CTAs).  Any output may be NULL. */
+cf_status cf_decode_plan(int n, const int* n_keys, int page_stride, int n_kv_heads, int plan_ctas, int* chunk,
+                         int* items, long long* max_items);
+
 /* The work plan of one prefill launch (host only; needs no GPU), as the
  * layer step and cf_prefill_attn_varlen make it for n chunks (len[i],
  * prefix[i]) given in stacked-row order on `sms` SMs.  *kind: the work unit,
