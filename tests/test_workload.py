@@ -1,7 +1,7 @@
 """CPU checks of the synthetic input recipe against the figures the pages fix.
 
 The decode-heavy mix stands in for the Mooncake Toolagent trace, whose prompt
-lengths ConfluxServe §8.1 (Table 3) reports as P50 6,346 and P95 26,114
+lengths ConfluxServe §8 (Table 3) reports as P50 6,346 and P95 26,114
 tokens.  The recipe draws clip(rint(exp(N(ln 6346, 0.86))), 512, 32768):
 0.86 = ln(26114 / 6346) / 1.645 puts the log-normal's 95th percentile on the
 trace's."""
