@@ -1,4 +1,4 @@
-"""CPU checks of the synthetic input recipe against the figures the pages fix.
+"""CPU checks of the synthetic input recipe against the trace figures ConfluxServe reports.
 
 The decode-heavy mix stands in for the Mooncake Toolagent trace, whose prompt
 lengths ConfluxServe §8 (Table 3) reports as P50 6,346 and P95 26,114
