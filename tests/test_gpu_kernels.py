@@ -194,6 +194,8 @@ DECODE_CASES = [
     ("q14b", wl.QWEN14B, (33, 1000, 15)),
     ("q32b", wl.QWEN32B, (3000, 31, 64)),
     ("g16", wl.LayerShape(2048, 32, 2, 64, 512, 1e4, 1e-5, False), (90, 1, 300)),
+    # one long request: ~250 chunks, so the merge reads (m, l) beyond the 64 it keeps in registers
+    ("long1", wl.LLAMA8B, (20000,)),
 ]
 
 
