@@ -611,11 +611,6 @@ constexpr int kMaxSplit = 13;
 
 }  // namespace
 
-int gemm_block_n(int epi) {
-  (void)epi;
-  return kGemmBN;
-}
-
 // split_mode: 0 automatic, 1 whole tiles only, >= 2 that many k-chunks per
 // tail tile (at most what fits in one wave).
 GemmSchedule gemm_schedule(int M, int N, int K, int epi, int ctas, int split_mode) {

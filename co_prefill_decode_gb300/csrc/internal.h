@@ -96,7 +96,6 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, 
 // describe B [N][K]; for SwiGLU B0 = gate and B1 = up.
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB0, const CUtensorMap& tmB1,
                         const GemmArgs& a, int num_sms, cudaStream_t s);
-int gemm_block_n(int epi);   // BN used for an epilogue kind
 
 // ------------------------------------------------------------------ row kernels
 // ------------------------------------------------------------------ prefill chunks
