@@ -420,6 +420,29 @@ def test_layer_rejects_bad_arguments(cf):
         S.eng.cf_layer_step(S.batch, S.x, S.x, S.pool)      # in place is not allowed
 
 
+def test_empty_calls_launch_nothing(cf):
+    """Degenerate batches: no decodes and no chunk (T = 0), a GEMM with no
+    rows and a decode call with no requests return at once, launch no
+    kernel and write nothing."""
+    w = wl.reduced(wl.WORKLOADS["tiny"], (17,), 8, 0)
+    S = LayerSetup(w)
+    S.out.fill_(7.0)
+    n0 = S.eng.cf_launch_count()
+    S.eng.cf_layer_step(cf.batch_of(0, S.dec_ctx, S.dec_pages, 0, 0, S.pre_pages), S.x, S.out, S.pool)
+    A = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    B = torch.randn(256, 256, device="cuda").bfloat16()
+    C = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    S.eng.cf_gemm(A, B, C)
+    s = S.s
+    q = torch.empty(0, s.n_q_heads, s.head_dim, dtype=torch.bfloat16, device="cuda")
+    S.eng.cf_decode_attn(q, s.n_q_heads * s.head_dim, S.pool, 0, S.dec_ctx, S.dec_pages, S.b.dec_stride, q,
+                         s.n_q_heads * s.head_dim)
+    torch.cuda.synchronize()
+    assert S.eng.cf_launch_count() == n0
+    assert bool((S.out.float() == 7.0).all())
+    assert S.eng.cf_get_error()[0] == 0
+
+
 def test_layer_step_is_deterministic_and_launch_count(cf):
     S = LayerSetup(wl.reduced(wl.WORKLOADS["q14b"], (100, 9), 50, 10))
     n0 = S.eng.cf_launch_count()
