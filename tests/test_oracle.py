@@ -446,3 +446,166 @@ def test_oracle_chain_sensitivity(monkeypatch):
     e = np.abs(got["out"] - ref["out"]) / np.maximum(1.0, np.abs(ref["out"]))
     assert 2e-3 < e.max() < 0.1 and e.mean() < 1e-2
 
+
+
+# ------------------------------------------------------------------ attention over paged caches
+def _place_requests(rng, n_keys, Hkv, d, ps, spare_pages=3):
+    """Contiguous per-request caches [n, Hkv, d] and the same values placed
+    token by token (brute force) through shuffled page tables into NaN-filled
+    pools [num_pages, Hkv, ps, d]; slots no request owns stay NaN, so a
+    gather that reads one key too many poisons the result."""
+    need = [(n + ps - 1) // ps for n in n_keys]
+    num_pages = sum(need) + spare_pages
+    perm = rng.permutation(num_pages)
+    stride = max(need + [1])
+    tables = np.full((len(n_keys), stride), -1, np.int64)
+    kpool = np.full((num_pages, Hkv, ps, d), np.nan)
+    vpool = np.full((num_pages, Hkv, ps, d), np.nan)
+    Ks, Vs, at = [], [], 0
+    for j, n in enumerate(n_keys):
+        tables[j, :need[j]] = perm[at:at + need[j]]
+        at += need[j]
+        K = rng.normal(size=(n, Hkv, d))
+        V = rng.normal(size=(n, Hkv, d))
+        for p in range(n):
+            page, off = tables[j, p // ps], p % ps
+            kpool[page, :, off, :] = K[p]
+            vpool[page, :, off, :] = V[p]
+        Ks.append(K)
+        Vs.append(V)
+    return Ks, Vs, kpool, vpool, tables
+
+
+def test_decode_attention_equals_brute_force_over_placed_cache():
+    """oracle.decode_attention (request j's single query at position n_j - 1
+    over its n_j keys, read through its page table) equals brute-force
+    attention over the contiguous cache.  Tiny-layer sizes (4/2 heads, d 64,
+    page 16); key counts cover one key (c = 0), a page-crossing context
+    (17 = one page + 1), a context ending exactly on a page (64), the next
+    page's first slot (65) and a full 16-page request (256)."""
+    rng = np.random.default_rng(11)
+    Hq, Hkv, d, ps = 4, 2, 64, 16
+    n_keys = [1, 17, 64, 65, 100, 256]
+    Ks, Vs, kpool, vpool, tables = _place_requests(rng, n_keys, Hkv, d, ps)
+    q = rng.normal(size=(len(n_keys), Hq, d))
+    got = oracle.decode_attention(q, kpool, vpool, np.array(n_keys), tables, ps)
+    assert np.isfinite(got).all()
+    for j, n in enumerate(n_keys):
+        want = brute_attention(q[j:j + 1], Ks[j], Vs[j], [n - 1])
+        assert np.allclose(got[j:j + 1], want, rtol=0, atol=1e-12), j
+    # one key: the output is that key's value row, for every query head
+    G = Hq // Hkv
+    for h in range(Hq):
+        assert np.array_equal(got[0, h], Vs[0][0, h // G])
+
+
+def test_prefill_attention_equals_brute_force_over_placed_cache():
+    """oracle.prefill_attention: chunk query i at position prefix + i sees
+    keys 0..prefix + i of its request, read through the page table.  The
+    tiny layer's own chunk (64 on a 128-token prefix) and chunks whose prefix
+    or end is not page-aligned, with no prefix, and of one token."""
+    rng = np.random.default_rng(12)
+    Hq, Hkv, d, ps = 4, 2, 64, 16
+    for prefix, l in ((128, 64), (37, 11), (0, 20), (16, 16), (250, 1)):
+        (K,), (V,), kpool, vpool, tables = _place_requests(rng, [prefix + l], Hkv, d, ps)
+        q = rng.normal(size=(l, Hq, d))
+        got = oracle.prefill_attention(q, kpool, vpool, prefix, tables[0], ps)
+        want = brute_attention(q, K, V, prefix + np.arange(l))
+        assert np.isfinite(got).all()
+        assert np.allclose(got, want, rtol=0, atol=1e-12), (prefix, l)
+
+
+# ------------------------------------------------------------------ layer wiring
+# A layer shape whose projections are not square: Hq d = 512 != H = 256 and
+# F = 512 != H, so a transposed W_o or W_down either fails to multiply or
+# moves a one-hot entry to another index.
+NONSQUARE = wl.LayerShape(256, 8, 2, 64, 512, 1.0e4, 1e-5, False)
+NONSQUARE_W = wl.Workload("nonsquare", NONSQUARE, 2, (5, 40), 24, 16, description="non-square projections")
+
+
+def _nonsquare(constant_x=None):
+    w = NONSQUARE_W
+    b = wl.make_batch(w)
+    x = oracle.to_f64(wl.make_x(w, b))
+    if constant_x is not None:
+        x[:] = constant_x
+    W = oracle.LayerWeights64.from_torch(wl.make_weights(w, unit_gains=True))
+    kp, vp = (oracle.to_f64(t) for t in wl.make_pools(w, b))
+    return w, b, x, W, kp, vp
+
+
+def test_oproj_orientation_on_a_non_square_layer():
+    """h = x + O_cat W_o^T with W_o in nn.Linear layout [H][Hq d]: a one-hot
+    W_o[i, j] adds attention feature j (head j // d, dim j % d) to hidden
+    feature i of every row and leaves every other feature of h equal to x.
+    j >= H, so W_o used untransposed cannot reach it."""
+    w, b, x, W, kp, vp = _nonsquare()
+    d = NONSQUARE.head_dim
+    i, j = 5, 300
+    W.w_o[:] = 0.0
+    W.w_o[i, j] = 1.0
+    r = oracle.layer_step(x, W, w.shape, b, kp, vp)
+    a = r["attn"][:, j // d, j % d]
+    assert np.abs(a).max() > 0.1
+    assert np.allclose(r["h"][:, i] - x[:, i], a, rtol=0, atol=1e-12)
+    others = np.arange(NONSQUARE.hidden) != i
+    assert np.array_equal(r["h"][:, others], x[:, others])
+
+
+def test_ffn_gate_and_up_roles_closed_form():
+    """out = h + (silu(hn W_gate^T) * (hn W_up^T)) W_down^T with the roles
+    fixed: with W_o = 0 (h = x), constant rows x = 1 and unit gains, hn is
+    exactly 1; a gate row of a / H and an up row of b / H then give gate
+    a and up b on unit f, whose activation silu(a) b reaches hidden feature
+    i through W_down[i, f] = 1 (nn.Linear layout [H][F], f >= H).  With
+    a = -8, b = 4 the activation is silu(-8) 4 ~ -0.011; swapping the roles
+    would give silu(4) (-8) ~ -31."""
+    w, b, x, W, kp, vp = _nonsquare(constant_x=1.0)
+    H, F = NONSQUARE.hidden, NONSQUARE.ffn_dim
+    f, i, a, bb = 300, 7, -8.0, 4.0
+    W.w_o[:] = 0.0
+    W.w_gate[:] = 0.0
+    W.w_up[:] = 0.0
+    W.w_down[:] = 0.0
+    W.w_gate[f, :] = a / H
+    W.w_up[f, :] = bb / H
+    W.w_down[i, f] = 1.0
+    r = oracle.layer_step(x, W, w.shape, b, kp, vp)
+    assert np.array_equal(r["hn"], np.ones_like(r["hn"]))
+    act = float(oracle.bf16_round(np.array([a * expit(a) * bb]))[0])
+    assert abs(act + 0.0107) < 1e-3
+    want = np.zeros_like(r["act"])
+    want[:, f] = act
+    assert np.array_equal(r["act"], want)
+    out_i = float(oracle.bf16_round(np.array([1.0 + act]))[0])
+    assert np.array_equal(r["out"][:, i], np.full(r["out"].shape[0], out_i))
+    others = np.arange(H) != i
+    assert np.array_equal(r["out"][:, others], x[:, others])
+
+
+def test_qkv_split_order_q_then_k_then_v():
+    """The fused projection's rows are the Q heads, then the K heads, then the
+    V heads (Decode Token Parallelism §4.4, Eq. 1).  With constant rows x = 1
+    and unit gains xn is exactly 1, so a W_qkv that is zero except row t
+    (value v / H) makes output feature t equal v and every other zero; at
+    position 0 (the first row of a chunk with no prefix) RoPE is the
+    identity, so exactly one element of q, k or v is non-zero, at the head
+    and dimension that row t names."""
+    s = NONSQUARE
+    w = wl.Workload("nonsquare-p0", s, 0, (), 8, 0)
+    b = wl.make_batch(w)
+    x = np.ones((b.n_tokens, s.hidden))
+    W = oracle.LayerWeights64.from_torch(wl.make_weights(w, unit_gains=True))
+    kp, vp = (oracle.to_f64(t) for t in wl.make_pools(w, b))
+    Hq, Hkv, d, H = s.n_q_heads, s.n_kv_heads, s.head_dim, s.hidden
+    cases = [("q", 3 * d + 5, (3, 5)), ("k", Hq * d + 1 * d + 7, (1, 7)), ("v", (Hq + Hkv) * d + 9, (0, 9)),
+             ("v", (Hq + Hkv) * d + d + 63, (1, 63))]
+    for name, t, (head, dim) in cases:
+        W.w_qkv[:] = 0.0
+        W.w_qkv[t, :] = 2.0 / H
+        r = oracle.layer_step(x, W, w.shape, b, kp, vp, rows=[0])
+        for key in ("q", "k", "v"):
+            want = np.zeros_like(r[key][0])
+            if key == name:
+                want[head, dim] = 2.0
+            assert np.array_equal(r[key][0], want), (name, key)
