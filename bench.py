@@ -33,12 +33,20 @@ sys.path.insert(0, ROOT)
 
 METRIC = "co-batched layer step µs & tokens/s; decode attn % HBM peak; GEMM % BF16 peak"
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
-# capture of the same shape; set to None whenever that kernel changes.
-# DRAM bytes (read + write) per launch of the roofline kernel, from one ncu
-# capture of the same kernel build; cleared whenever that kernel changes.
-DOMINANT_TRAFFIC = {
-    "l8b": {"bytes": 243638528 + 22196480, "source": "profiles/gemm_gateup_l8b_T1040.md"},
+# DRAM bytes (read + write) per launch of each workload's roofline kernel,
+# from one ncu capture of that kernel build at that shape (the summary named
+# in "source"); an entry is removed whenever its kernel changes.
+DOMINANT_TRAFFIC = {}
+
+# The kernels of a step that a roofline can name: phase of the engine's
+# per-phase timers, bound, and what the roofline object calls it.
+ROOFLINE_KERNELS = {
+    "qkv": ("tensor", "fused QKV GEMM + QK-norm/RoPE/KV-append epilogue"),
+    "oproj": ("tensor", "O-proj GEMM + residual"),
+    "gateup": ("tensor", "gate/up GEMM + SwiGLU epilogue"),
+    "down": ("tensor", "down GEMM + residual"),
+    "decode": ("hbm", "split-K decode attention over paged KV"),
+    "prefill": ("tensor", "causal chunked-prefill attention (tcgen05)"),
 }
 
 
@@ -264,13 +272,11 @@ def run_cf(args, rank, world, local, pg):
         raise RuntimeError(msg)
     calib = None
     if args.decode_sms == 0 and b.n_decode > 0 and b.prefill_rows > 0:
-        # ConfluxServe §6.1: decode gets the fewest SMs that keep 90% of its solo bandwidth
-        chosen = eng.cf_calibrate_decode_sms(batch, pool, 0.9)
-        calib = {"rule": "min SMs reaching 90% of standalone decode bandwidth", "chosen": chosen,
+        # ConfluxServe §6.1: decode gets the fewest SMs that keep 90% of its
+        # solo bandwidth; the library measured it on the first warm-up step
+        calib = {"rule": "min SMs reaching 90% of standalone decode bandwidth (measured by the library on "
+                         "the first step of the batch's bucket)", "chosen": eng.cf_engine_decode_sms(),
                  "points": [{"sms": n, "ms": round(t, 4)} for n, t in eng.cf_calibration_points()]}
-        for _ in range(2):
-            step()
-        torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -365,6 +371,36 @@ def run_cf(args, rank, world, local, pg):
     if st != 0:
         raise RuntimeError(msg)
 
+    # Serialized execution (ConfluxServe §8.3, Fig. 14a): decode alone on all
+    # SMs, then prefill alone on all SMs, same kernels and items.  Its phase
+    # times give each path's isolated time; the larger one is the
+    # contention-free bound of the fork.
+    serial = None
+    if b.n_decode > 0 and b.prefill_rows > 0:
+        eng.cf_set_fork_mode(1)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ns = min(args.steps, 50)
+        s0.record(stream)
+        for _ in range(ns):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        step_serial_ms = s0.elapsed_time(s1) / ns
+        eng.cf_set_profiling(True)
+        eng.cf_get_phase_times()
+        for _ in range(ns):
+            step()
+        torch.cuda.synchronize()
+        sph, sn = eng.cf_get_phase_times()
+        eng.cf_set_profiling(False)
+        eng.cf_set_fork_mode(0)
+        sp = {k: v / max(sn, 1) for k, v in sph.items()}
+        serial = {"step_ms": step_serial_ms, "attention_ms": sp["fork"], "decode_alone_ms": sp["decode"],
+                  "prefill_alone_ms": sp["prefill"]}
+
     peaks = load_peaks()
     wk = work_of(w, b)
     per = {k: v / max(nsteps, 1) for k, v in phases.items()}   # ms per step
@@ -381,8 +417,24 @@ def run_cf(args, rank, world, local, pg):
                            "sms": eng.cf_engine_decode_sms()}
     kern["prefill_attn"] = {"ms": per["prefill"],
                             "tflops": wk["prefill_flops"] / t_pre / 1e12 if t_pre > 0 else None}
-    kern["fork"] = {"ms": per["fork"], "serial_ms": per["decode"] + per["prefill"],
-                    "to_decode_start_ms": per.get("fork_in"), "decode_end_to_join_ms": per.get("fork_out")}
+    kern["fork"] = {"ms": per["fork"], "to_decode_start_ms": per.get("fork_in"),
+                    "decode_end_to_join_ms": per.get("fork_out")}
+    fork_cmp = None
+    if serial is not None:
+        # fork vs serialized execution and the contention-free bound
+        bound = max(serial["decode_alone_ms"], serial["prefill_alone_ms"])
+        gap = serial["attention_ms"] - bound
+        fork_cmp = {"fork_ms": per["fork"], "serial_ms": serial["attention_ms"], "isolated_max_ms": bound,
+                    "decode_alone_ms": serial["decode_alone_ms"], "prefill_alone_ms": serial["prefill_alone_ms"],
+                    "fork_vs_serial": per["fork"] / serial["attention_ms"],
+                    "gap_closed": (serial["attention_ms"] - per["fork"]) / gap if gap > 0 else None,
+                    "step_ms_fork": ms_step, "step_ms_serial": serial["step_ms"],
+                    "method": "attention region (QKV end to join) between CUDA events, per-phase pass of "
+                              f"{min(args.steps, 50)} steps per mode; serial = decode then prefill, each alone on "
+                              "all SMs, same kernels and work items"}
+        t_dec_iso, t_pre_iso = serial["decode_alone_ms"] / 1e3, serial["prefill_alone_ms"] / 1e3
+        kern["decode_attn"]["alone_gbs"] = wk["decode_bytes"] / t_dec_iso / 1e9 if t_dec_iso > 0 else None
+        kern["prefill_attn"]["alone_tflops"] = wk["prefill_flops"] / t_pre_iso / 1e12 if t_pre_iso > 0 else None
     kern["rmsnorm"] = {"ms": per["rmsnorm"] + per["rmsnorm2"]}
     gemm_ms = sum(per[k] for k in ("qkv", "oproj", "gateup", "down"))
     gemm_tflops = sum(wk["gemm_flops"].values()) / (gemm_ms / 1e3) / 1e12
@@ -390,15 +442,35 @@ def run_cf(args, rank, world, local, pg):
     # the fractions use the measured burst bf16 peak (the larger, stricter
     # denominator); the sustained power-capped figure is reported beside it.
     peak_tc = peaks["bf16_tflops"]
-    dom = kern["gateup"]
-    traffic = DOMINANT_TRAFFIC.get(args.workload)
-    roofline = {"kernel": "gate/up GEMM + SwiGLU epilogue", "bound": "tensor",
-                "achieved": dom["tflops"], "peak": peak_tc, "unit": "TFLOP/s",
-                "frac": dom["tflops"] / peak_tc if dom["tflops"] else None,
-                "traffic": traffic["bytes"] if traffic else None,
-                "algorithmic_bytes": wk["weight_bytes"]["gateup"] + 2.0 * T * s_hidden(w) + 2.0 * T * w.shape.ffn_dim,
-                "peak_source": peaks["source"] + " burst bf16 (sustained: %.0f)" % peaks["bf16_tflops_sustained"],
-                "traffic_source": traffic["source"] if traffic else None}
+    # the roofline kernel: the one with the largest share of the step's time
+    # (per-phase CUDA events on the stream each kernel runs on)
+    dom_phase = max((k for k in ROOFLINE_KERNELS if per.get(k, 0) > 0), key=lambda k: per[k])
+    bound, kname = ROOFLINE_KERNELS[dom_phase]
+    t_dom = per[dom_phase] / 1e3
+    if bound == "hbm":
+        work_dom = wk["decode_bytes"]
+        achieved, peak, unit = work_dom / t_dom / 1e9, peaks["hbm_gbs"], "GB/s"
+        peak_src = peaks["source"] + " HBM copy bandwidth"
+        algo_bytes = work_dom
+    else:
+        work_dom = wk["prefill_flops"] if dom_phase == "prefill" else wk["gemm_flops"][dom_phase]
+        achieved, peak, unit = work_dom / t_dom / 1e12, peak_tc, "TFLOP/s"
+        peak_src = peaks["source"] + " burst bf16 (sustained: %.0f)" % peaks["bf16_tflops_sustained"]
+        if dom_phase == "prefill":   # each request's K and V read once, Q read and O written
+            algo_bytes = sum((c + l) * w.shape.n_kv_heads * w.shape.head_dim * 4 for l, c, _ in b.chunks) + \
+                b.prefill_rows * w.shape.n_q_heads * w.shape.head_dim * 4
+        else:
+            n_out = {"qkv": w.shape.qkv_dim, "oproj": s_hidden(w), "gateup": w.shape.ffn_dim, "down": s_hidden(w)}
+            k_in = {"qkv": s_hidden(w), "oproj": w.shape.n_q_heads * w.shape.head_dim, "gateup": s_hidden(w),
+                    "down": w.shape.ffn_dim}
+            algo_bytes = wk["weight_bytes"][dom_phase] + 2.0 * T * (k_in[dom_phase] + n_out[dom_phase])
+    traffic = DOMINANT_TRAFFIC.get((args.workload, dom_phase))
+    roofline = {"kernel": kname, "phase": dom_phase, "bound": bound, "achieved": achieved, "peak": peak,
+                "unit": unit, "frac": achieved / peak, "share_of_step": per[dom_phase] / max(1e-9, per["step"]),
+                "work_per_launch": work_dom, "launch_ms": per[dom_phase],
+                "traffic": traffic["bytes"] if traffic else None, "algorithmic_bytes": algo_bytes,
+                "peak_source": peak_src, "traffic_source": traffic["source"] if traffic else None,
+                "timing": "CUDA events around the kernel on its stream, per-phase pass after the timed region"}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "layer_step_us": ms_step * 1e3,
@@ -411,7 +483,8 @@ def run_cf(args, rank, world, local, pg):
         "gemm_bf16_frac": gemm_tflops / peak_tc,
         "prefill_attn_bf16_frac": (kern["prefill_attn"]["tflops"] or 0) / peak_tc,
         "gemm_tflops": gemm_tflops,
-        "fork_vs_serial": per["fork"] / max(1e-9, per["decode"] + per["prefill"]),
+        "fork_vs_serial": fork_cmp["fork_vs_serial"] if fork_cmp else None,
+        "fork_vs_serial_detail": fork_cmp,
         "kernels": kern,
         "decode_sms_calibration": calib,
         "roofline": roofline,
@@ -432,13 +505,20 @@ def run_cf(args, rank, world, local, pg):
                                 "kind": "oracle", "host_cores": os.cpu_count(),
                                 "sample": f"fp64 oracle layer step on {len(rows)} of {T} rows (first 64 rows of the "
                                           f"first chunk + all decodes), {reps} repetitions, {secs:.1f} s"}
-    if args.sweep_decode_sms:
-        line["decode_sms_sweep"] = sweep_decode_sms(eng, step, args, cf)
+    if b.n_decode > 0 and b.prefill_rows > 0 and not args.no_share_sweep:
+        # the share the rule picks against the share that minimises the fork
+        sw = sweep_decode_sms(eng, step, args, cf, reps=10 if not args.sweep_decode_sms else None)
+        best = min(sw, key=lambda r: r["fork"])
+        line["decode_share_sweep"] = {"rule_sms": eng.cf_engine_decode_sms(), "rule_fork_ms": per["fork"],
+                                      "best_sms": best["decode_sms"], "best_fork_ms": best["fork"],
+                                      "points": [{"sms": r["decode_sms"], "frac": r["frac"], "fork_ms": r["fork"]}
+                                                 for r in sw]}
     eng.close()
     return line
 
 
-def sweep_decode_sms(eng, step, args, cf):
+def sweep_decode_sms(eng, step, args, cf, reps=None):
+    """Fork time (per-phase events) at decode shares of 10% .. 50% of the SMs."""
     import torch
     sms = cf.device_sm_count()
     res = []
@@ -449,7 +529,7 @@ def sweep_decode_sms(eng, step, args, cf):
             step()
         eng.cf_set_profiling(True)
         eng.cf_get_phase_times()
-        for _ in range(max(5, args.steps // 4)):
+        for _ in range(reps or max(5, args.steps // 4)):
             step()
         ph, ns = eng.cf_get_phase_times()
         eng.cf_set_profiling(False)
@@ -466,6 +546,8 @@ def run_kernel_case(args):
              (268 MB of KV, larger than L2)
     prefill: prefill attention, Qwen3-32B shape, 2048-token chunk on 4096 cached
              (8 query-tile pairs x 64 heads: several waves of paired items)
+    prefill-long: prefill attention of the Qwen3-32B step, 4096-token chunk on
+             28672 cached (1.1 GB of K/V in the pools)
     gemm   : gate/up GEMM + SwiGLU epilogue of the Llama-3.1-8B layer, T = 1040
     prefill-chunks: prefill attention over four chunks of different requests in
              one launch, Llama-3.1-8B shape, (l, c) = (1024, 0), (512, 4096),
@@ -482,6 +564,8 @@ def run_kernel_case(args):
         w = wl.Workload("k", s, 8, (8192,) * 8, 0, 0)
     elif which == "prefill":
         w = wl.Workload("k", s, 0, (), 2048, 4096)
+    elif which == "prefill-long":
+        w = wl.Workload("k", s, 0, (), 4096, 28672)
     elif which == "prefill-chunks":
         w = wl.Workload("k", s, 0, (), 1024, 0, more_chunks=((512, 4096), (256, 12288), (128, 2048)))
     else:
@@ -493,7 +577,7 @@ def run_kernel_case(args):
     pool = cf.pool_of(kp, vp)
     Hq, d = s.n_q_heads, s.head_dim
     g = torch.Generator(device="cuda").manual_seed(args.seed)
-    if which in ("prefill", "prefill-chunks"):
+    if which in ("prefill", "prefill-long", "prefill-chunks"):
         for l, cp, pages in b.chunks:   # each chunk's own K/V
             pos = np.arange(cp, cp + l)
             pg = torch.as_tensor(pages[pos // 16].astype(np.int64), device="cuda")
@@ -506,7 +590,7 @@ def run_kernel_case(args):
             o = torch.empty_like(q)
             eng.cf_decode_attn(q, Hq * d, pool, b.n_decode, torch.as_tensor(b.dec_ctx, device="cuda"),
                                torch.as_tensor(b.dec_pages, device="cuda"), b.dec_stride, o, Hq * d)
-        elif which == "prefill":
+        elif which in ("prefill", "prefill-long"):
             q = torch.randn(b.prefill_len, Hq, d, device="cuda", generator=g).bfloat16()
             o = torch.empty_like(q)
             eng.cf_prefill_attn(q, pool, b.prefill_len, b.prefill_prefix, torch.as_tensor(b.pre_pages, device="cuda"), o)
@@ -756,11 +840,14 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="l8b")
+    ap.add_argument("--workload", default="q32b",
+                    help="tiny | l8b | q14b | mix | q32b (default: the largest single-GPU configuration) | mchunk")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="cf", choices=["cf", "reference"])
     ap.add_argument("--decode-sms", type=int, default=0)
-    ap.add_argument("--sweep-decode-sms", action="store_true")
+    ap.add_argument("--sweep-decode-sms", action="store_true",
+                    help="longer decode-share sweep (steps/4 profiled steps per share instead of 10)")
+    ap.add_argument("--no-share-sweep", action="store_true", help="skip the decode-share sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graphs", type=int, default=0, choices=[0, 1],
                     help="replay the linear segments of the step as CUDA graphs (1) or launch eagerly (0)")
@@ -770,7 +857,7 @@ def main(argv=None):
                     help="prefill key-range cuts: 0 automatic, 1 never, n >= 2 n ranges")
     ap.add_argument("--split-k", type=int, default=0,
                     help="GEMM split-K tail: 0 automatic, 1 whole tiles only, n >= 2 n k-chunks")
-    ap.add_argument("--kernel", choices=["decode", "prefill", "gemm", "prefill-chunks"], default=None,
+    ap.add_argument("--kernel", choices=["decode", "prefill", "prefill-long", "gemm", "prefill-chunks"], default=None,
                     help="run one small launch of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--estimator", default=None,
                     help="fit and validate the iteration-latency estimator for these workloads "

@@ -31,7 +31,7 @@ EXPORTS = (
     "cf_launch_count", "cf_rmsnorm", "cf_qkv", "cf_decode_attn_noalloc", "cf_calibrate_decode_sms",
     "cf_calibration_points", "cf_gemm_schedule", "cf_set_split_k", "cf_prefill_plan", "cf_decode_plan", "cf_selftest_timeout", "cf_set_prefill_pairing", "cf_set_graphs", "cf_graph_captures",
     "cf_latency_predict", "cf_latency_fit_line", "cf_latency_calibrate", "cf_waterfill_dispatch",
-    "cf_waterfill_assign", "cf_prefill_attn_varlen", "cf_set_prefill_split",
+    "cf_waterfill_assign", "cf_prefill_attn_varlen", "cf_set_prefill_split", "cf_set_fork_mode",
 )
 
 
@@ -135,6 +135,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_set_prefill_pairing": (I, [P, I]),
         "cf_set_prefill_split": (I, [P, I]),
         "cf_set_graphs": (I, [P, I]),
+        "cf_set_fork_mode": (I, [P, I]),
         "cf_graph_captures": (L, [P]),
         "cf_latency_predict": (I, [ctypes.POINTER(cf_latency_model), I, ctypes.POINTER(cf_rank_load), I,
                                    ctypes.POINTER(L), ctypes.POINTER(L), I, ctypes.POINTER(cf_latency_parts)]),
@@ -330,6 +331,10 @@ class Engine:
 
     def cf_set_graphs(self, on: bool):
         _check(self.lib, self.handle, self.lib.cf_set_graphs(self.handle, int(on)))
+
+    def cf_set_fork_mode(self, mode: int):
+        """0: concurrent work-conserving attention fork; 1: serial (decode, then prefill, each on all SMs)."""
+        _check(self.lib, self.handle, self.lib.cf_set_fork_mode(self.handle, int(mode)))
 
     def cf_graph_captures(self) -> int:
         return int(self.lib.cf_graph_captures(self.handle))

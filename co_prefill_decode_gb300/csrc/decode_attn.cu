@@ -570,13 +570,9 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
 
 template <int D, bool G16>
 cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int ctas, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kDecodeSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = smem_limit_per_device(decode_kernel<D, G16>, kDecodeSmem, attr);
+  if (e != cudaSuccess) return e;
   if (a.pdl) return launch_pdl(decode_kernel<D, G16>, dim3(ctas), dim3(kThreads), kDecodeSmem, s, tk, tv, a);
   decode_kernel<D, G16><<<ctas, kThreads, kDecodeSmem, s>>>(tk, tv, a);
   return cudaGetLastError();

@@ -75,11 +75,13 @@ extern "C" cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int h
   if (ctas > sms) ctas = sms;
 
   // Scratch layout: error word (byte 0) and work-queue counter (byte 128) |
-  // chunk plan | (m, l) partials | O partials.  The counter must be 0 when a
-  // call starts: it is 0 when the library is loaded and the merge kernel of
-  // every call sets it back to 0.
+  // chunk plan | (m, l) partials | O partials.  Both words are cleared on the
+  // call's stream before the kernel runs, so a call never depends on how the
+  // previous one ended.  The keys are cut into chunks planned for the CTAs
+  // this call launches, so a smaller num_sms needs less scratch (with all SMs
+  // the plan, and so the output, is the one cf_decode_attn makes).
   const int G = n_q_heads / n_kv_heads;
-  const long long items = decode_max_items(n, n_kv_heads, sms);
+  const long long items = decode_max_items(n, n_kv_heads, ctas);
   const size_t off_plan = 256;
   const size_t off_ml = align256(off_plan + (size_t)(n + 4) * 4);
   const size_t off_o = align256(off_ml + (size_t)items * G * 2 * 4);
@@ -119,7 +121,9 @@ extern "C" cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int h
   da.part_ml = reinterpret_cast<float*>(b + off_ml);
   da.part_o = reinterpret_cast<float*>(b + off_o);
   da.max_items = items;
-  da.plan_ctas = sms;
+  da.plan_ctas = ctas;
   da.wait_ns = 2000000000ull;
-  return launch_decode(tk, tv, da, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(b, 0, 256, s) != cudaSuccess) return CF_ERR_CUDA;
+  return launch_decode(tk, tv, da, ctas, s) == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }

@@ -85,6 +85,14 @@ using namespace cf;
 namespace {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s cap on any one device wait
+// Decode batches are bucketed by ceil(log2 n_decode) (n_decode <= 2048) for
+// the automatic SM share: each bucket is calibrated on its first step.
+constexpr int kBuckets = 12;
+int bucket_of(int n_decode) {
+  int b = 0;
+  while ((1 << b) < n_decode && b < kBuckets - 1) ++b;
+  return b;
+}
 constexpr int kPhases = 12;
 constexpr int kRing = 64;
 enum { PH_PREP = 0, PH_QKV, PH_DEC, PH_PRE, PH_FORK, PH_OPROJ, PH_PREP2, PH_GU, PH_DOWN, PH_STEP, PH_FORK_IN,
@@ -111,7 +119,10 @@ struct cf_engine {
   cf_config cfg;
   cf_weights w;
   int dev = 0, sms = 0;
-  int decode_sms = 0;            // 0: auto
+  int decode_sms = 0;            // explicit share (cf_set_decode_sms); 0: the config's, else auto
+  int fork_mode = 0;             // 0: concurrent work-conserving fork; 1: serial (decode, then prefill)
+  int auto_sms[kBuckets] = {0};  // the 90%-rule share per decode-batch bucket; 0: not measured yet
+  int last_bucket = -1;          // bucket of the last step with decodes
   cudaStream_t dstream = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_dec = nullptr;
   // workspace
@@ -200,10 +211,15 @@ cf_status check_config(const cf_config* c) {
   return CF_OK;
 }
 
-int pick_decode_sms(cf_engine* e, bool have_prefill, bool have_decode) {
+// The share is, in order: the explicit one (cf_set_decode_sms), the
+// configuration's, the measured 90%-rule share of the batch's bucket, and
+// before any measurement a third of the SMs.
+int pick_decode_sms(cf_engine* e, bool have_prefill, bool have_decode, int bucket) {
   if (!have_prefill) return e->sms;
   if (!have_decode) return 0;
-  int n = e->decode_sms > 0 ? e->decode_sms : (e->cfg.decode_sms > 0 ? e->cfg.decode_sms : e->sms / 3);
+  int n = e->decode_sms > 0 ? e->decode_sms : e->cfg.decode_sms;
+  if (n <= 0 && bucket >= 0 && bucket < kBuckets) n = e->auto_sms[bucket];
+  if (n <= 0) n = e->sms / 3;
   if (n < 1) n = 1;
   if (n > e->sms - 1) n = e->sms - 1;
   return n;
@@ -425,6 +441,88 @@ void prof_resolve(cf_engine* e, int slot) {
   e->phase_ms[PH_STEP] += el(EV_START, EV_END);
   e->phase_steps += 1;
   e->ring_used[slot] = 0;
+}
+
+// The decode attention of a step's batch: its Q rows (after the chunk rows
+// of the engine's Q buffer), its output rows of the attention buffer.
+DecodeArgs step_decode_args(cf_engine* e, const cf_batch* bt, int chunk_rows, const cf_kv_pool* pool) {
+  const cf_config& c = e->cfg;
+  const size_t row = (size_t)c.n_q_heads * c.head_dim;
+  DecodeArgs da{};
+  da.q = e->q + (size_t)chunk_rows * row;
+  da.q_stride = (long long)row;
+  da.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
+  da.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
+  da.num_pages = pool->num_pages;
+  da.n = bt->n_decode;
+  da.n_keys = bt->dec_ctx;
+  da.key_offset = 1;
+  da.pages = bt->dec_pages;
+  da.page_stride = bt->dec_stride;
+  da.out = e->attn + (size_t)chunk_rows * row;
+  da.out_stride = (long long)row;
+  da.Hq = c.n_q_heads;
+  da.Hkv = c.n_kv_heads;
+  da.head_dim = c.head_dim;
+  da.page_size = c.page_size;
+  da.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+  da.part_o = e->part_o;
+  da.part_ml = e->part_ml;
+  da.plan = e->plan;
+  da.max_items = e->max_items;
+  da.counter = e->dec_counter;
+  da.plan_ctas = e->sms;
+  da.wait_ns = kWaitNs;
+  da.err = e->err;
+  return da;
+}
+
+// ConfluxServe §6.1: decode gets "the minimum number of SMs needed to
+// sustain 90% of its standalone peak HBM bandwidth".  Times the decode
+// attention `da` alone (kernel + merge, on `s`) on 8, 16, ..., all SMs,
+// each point the median of three timed launches after a warm-up one, and
+// picks the smallest CTA count whose time is within 1/frac of the fastest.
+// Synchronous (waits for the work already queued on `s`); overwrites the
+// decode rows of `da.out` and the partials, which the caller recomputes.
+cf_status measure_decode_share(cf_engine* e, const DecodeArgs& da, cudaStream_t s, float frac, int* chosen) {
+  cudaEvent_t ev[4];
+  for (auto& x : ev) CF_CUDA(e, cudaEventCreate(&x));
+  std::vector<std::pair<int, float>> res;
+  cf_status st = CF_OK;
+  for (int n = 8;; n += 8) {
+    const int ctas = n < e->sms ? n : e->sms;
+    cudaError_t r = launch_decode(e->pm.tk, e->pm.tv, da, ctas, s);
+    for (int k = 0; k < 3 && r == cudaSuccess; ++k) {
+      r = cudaEventRecord(ev[k], s);
+      if (r == cudaSuccess) r = launch_decode(e->pm.tk, e->pm.tv, da, ctas, s);
+    }
+    if (r == cudaSuccess) r = cudaEventRecord(ev[3], s);
+    if (r == cudaSuccess) r = cudaEventSynchronize(ev[3]);
+    if (r != cudaSuccess) {
+      st = cuda_fail(e, r, "decode share calibration");
+      break;
+    }
+    float t[3];
+    for (int k = 0; k < 3; ++k) cudaEventElapsedTime(&t[k], ev[k], ev[k + 1]);
+    const float lo = fminf(t[0], fminf(t[1], t[2])), hi = fmaxf(t[0], fmaxf(t[1], t[2]));
+    res.push_back({ctas, t[0] + t[1] + t[2] - lo - hi});
+    e->launches += 8;
+    if (ctas == e->sms) break;
+  }
+  for (auto& x : ev) cudaEventDestroy(x);
+  if (st != CF_OK) return st;
+  float best = 1e30f;
+  for (auto& r : res) best = r.second < best ? r.second : best;
+  int pick = e->sms - 1;
+  for (auto& r : res)
+    if (best / r.second >= frac) {
+      pick = r.first;
+      break;
+    }
+  if (pick >= e->sms) pick = e->sms - 1;
+  e->calib.assign(res.begin(), res.end());
+  *chosen = pick;
+  return CF_OK;
 }
 
 }  // namespace
@@ -727,37 +825,13 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
   // whichever path finishes first launches a second grid of the other
   // kernel on its SMs, which takes the remaining items (or none).  Decode's
   // merge runs once both decode grids are done.
-  const int n_dec_sms = pick_decode_sms(e, l > 0, nd > 0);
-  const int n_pre_sms = e->sms - n_dec_sms;
   const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
   DecodeArgs da{};
   PrefillArgs pf{};
+  const int bucket = nd > 0 ? bucket_of(nd) : -1;
   if (nd > 0) {
-    da.q = e->q + (size_t)l * Hq * d;
-    da.q_stride = (long long)Hq * d;
-    da.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
-    da.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
-    da.num_pages = pool->num_pages;
-    da.n = nd;
-    da.n_keys = bt->dec_ctx;
-    da.key_offset = 1;
-    da.pages = bt->dec_pages;
-    da.page_stride = bt->dec_stride;
-    da.out = e->attn + (size_t)l * Hq * d;
-    da.out_stride = (long long)Hq * d;
-    da.Hq = Hq;
-    da.Hkv = c.n_kv_heads;
-    da.head_dim = d;
-    da.page_size = c.page_size;
-    da.scale_log2 = scale_log2;
-    da.part_o = e->part_o;
-    da.part_ml = e->part_ml;
-    da.plan = e->plan;
-    da.max_items = e->max_items;
-    da.counter = e->dec_counter;
-    da.plan_ctas = e->sms;
-    da.wait_ns = kWaitNs;
-    da.err = e->err;
+    da = step_decode_args(e, bt, l, pool);
+    e->last_bucket = bucket;
   }
   if (l > 0) {
     pf.Hq = Hq;
@@ -774,48 +848,86 @@ cf_status cf_layer_step(cf_engine* e, const cf_batch* bt, const void* x_in, void
     pf.err = e->err;
     pf.wait_ns = kWaitNs;
   }
-  if (nd > 0) {
-    CF_CUDA(e, cudaEventRecord(e->ev_fork, s));
-    CF_CUDA(e, cudaStreamWaitEvent(e->dstream, e->ev_fork, 0));
-    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC0], e->dstream));
-    CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, da, n_dec_sms, e->dstream));
-    e->launches++;
-    // every decode item has been taken when this grid ends (a second grid
-    // started later only takes items this one has not reached; it may still
-    // be finishing its last ones), so this is decode's time in the fork
-    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], e->dstream));
-    CF_CUDA(e, cudaEventRecord(e->ev_dec, e->dstream));
-    if (l > 0) {   // decode's SMs join prefill once decode is done
-      PrefillArgs helper = pf;
-      helper.pdl = 1;   // starts on each SM decode frees
-      CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, helper, n_dec_sms, e->dstream));
-      e->launches++;
-    }
-    CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
-  }
-  if (l > 0) {
-    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE0], s));
-    CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_pre_sms, s));
-    e->launches++;
-    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE1], s));
-    if (nd > 0) {   // prefill's SMs join decode once prefill is done
-      DecodeArgs helper = da;
-      helper.pdl = 1;   // starts on each SM prefill frees
-      CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, helper, n_pre_sms, s));
-      e->launches++;
+  // The automatic decode share: the first concurrent step of a decode-batch
+  // bucket measures the 90% rule on its own batch (synchronously, on
+  // `stream`, after its QKV stage) unless `stream` is being captured.
+  if (nd > 0 && l > 0 && e->fork_mode == 0 && e->decode_sms <= 0 && c.decode_sms <= 0 && !e->auto_sms[bucket]) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CF_CUDA(e, cudaStreamIsCapturing(s, &cs));
+    if (cs == cudaStreamCaptureStatusNone) {
+      int pick = 0;
+      st = measure_decode_share(e, da, s, 0.9f, &pick);
+      if (st != CF_OK) return st;
+      e->auto_sms[bucket] = pick;
     }
   }
-  if (nd > 0) {
-    CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_dec, 0));
-    CF_CUDA(e, launch_decode_merge(da, s));
-    e->launches++;
-    CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_join, 0));
+  const int n_dec_sms = pick_decode_sms(e, l > 0, nd > 0, bucket);
+  const int n_pre_sms = e->sms - n_dec_sms;
+  if (e->fork_mode == 1) {
+    // Serial execution (the baseline the fork is measured against,
+    // ConfluxServe §8.3): decode alone on all SMs, then prefill alone on
+    // all SMs, on `stream`, with the same kernels and work items.
+    if (nd > 0) {
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC0], s));
+      CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, e->sms, s));
+      e->launches += 2;
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], s));
+    }
+    if (l > 0) {
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE0], s));
+      CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, e->sms, s));
+      e->launches++;
+      if (prefill_merge_blocks(pf) > 0) {
+        CF_CUDA(e, launch_prefill_merge(pf, s));
+        e->launches++;
+      }
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE1], s));
+    }
+    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_JOIN], s));
+  } else {
+    if (nd > 0) {
+      CF_CUDA(e, cudaEventRecord(e->ev_fork, s));
+      CF_CUDA(e, cudaStreamWaitEvent(e->dstream, e->ev_fork, 0));
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC0], e->dstream));
+      CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, da, n_dec_sms, e->dstream));
+      e->launches++;
+      // every decode item has been taken when this grid ends (a second grid
+      // started later only takes items this one has not reached; it may still
+      // be finishing its last ones), so this is decode's time in the fork
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_DEC1], e->dstream));
+      CF_CUDA(e, cudaEventRecord(e->ev_dec, e->dstream));
+      if (l > 0) {   // decode's SMs join prefill once decode is done
+        PrefillArgs helper = pf;
+        helper.pdl = 1;   // starts on each SM decode frees
+        CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, helper, n_dec_sms, e->dstream));
+        e->launches++;
+      }
+      CF_CUDA(e, cudaEventRecord(e->ev_join, e->dstream));
+    }
+    if (l > 0) {
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE0], s));
+      CF_CUDA(e, launch_prefill(e->tm.q3, e->pm.tk, e->pm.tv, pf, n_pre_sms, s));
+      e->launches++;
+      if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_PRE1], s));
+      if (nd > 0) {   // prefill's SMs join decode once prefill is done
+        DecodeArgs helper = da;
+        helper.pdl = 1;   // starts on each SM prefill frees
+        CF_CUDA(e, launch_decode_kernel(e->pm.tk, e->pm.tv, helper, n_pre_sms, s));
+        e->launches++;
+      }
+    }
+    if (nd > 0) {
+      CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_dec, 0));
+      CF_CUDA(e, launch_decode_merge(da, s));
+      e->launches++;
+      CF_CUDA(e, cudaStreamWaitEvent(s, e->ev_join, 0));
+    }
+    if (l > 0 && prefill_merge_blocks(pf) > 0) {   // both prefill grids are done: merge the cut items
+      CF_CUDA(e, launch_prefill_merge(pf, s));
+      e->launches++;
+    }
+    if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_JOIN], s));
   }
-  if (l > 0 && prefill_merge_blocks(pf) > 0) {   // both prefill grids are done: merge the cut items
-    CF_CUDA(e, launch_prefill_merge(pf, s));
-    e->launches++;
-  }
-  if (ev) CF_CUDA(e, cudaEventRecord(ev[EV_JOIN], s));
 
   // a6 - a9
   if (ge) {
@@ -1190,7 +1302,13 @@ void* cf_engine_buffer(cf_engine* e, const char* name) {
   return nullptr;
 }
 
-int cf_engine_decode_sms(cf_engine* e) { return e ? pick_decode_sms(e, true, true) : 0; }
+int cf_engine_decode_sms(cf_engine* e) { return e ? pick_decode_sms(e, true, true, e->last_bucket) : 0; }
+
+cf_status cf_set_fork_mode(cf_engine* e, int mode) {
+  if (!e || mode < 0 || mode > 1) return CF_ERR_INVALID_ARG;
+  e->fork_mode = mode;
+  return CF_OK;
+}
 
 cf_status cf_set_decode_sms(cf_engine* e, int n) {
   if (!e || n < 0 || n >= e->sms) return CF_ERR_INVALID_ARG;
@@ -1209,75 +1327,12 @@ cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* bt, const cf_kv_
   if (st != CF_OK) return st;
   st = pool_maps(e, pool);
   if (st != CF_OK) return st;
-  const cf_config& c = e->cfg;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t row = (size_t)c.n_q_heads * c.head_dim;
-  DecodeArgs da{};
-  da.q = e->q + (size_t)ch.rows * row;   // Q rows of the last step's decodes
-  da.q_stride = (long long)row;
-  da.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
-  da.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
-  da.num_pages = pool->num_pages;
-  da.n = bt->n_decode;
-  da.n_keys = bt->dec_ctx;
-  da.key_offset = 1;
-  da.pages = bt->dec_pages;
-  da.page_stride = bt->dec_stride;
-  da.out = e->attn + (size_t)ch.rows * row;
-  da.out_stride = (long long)row;
-  da.Hq = c.n_q_heads;
-  da.Hkv = c.n_kv_heads;
-  da.head_dim = c.head_dim;
-  da.page_size = c.page_size;
-  da.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
-  da.part_o = e->part_o;
-  da.part_ml = e->part_ml;
-  da.plan = e->plan;
-  da.max_items = e->max_items;
-  da.counter = e->dec_counter;
-  da.plan_ctas = e->sms;
-  da.wait_ns = kWaitNs;
-  da.err = e->err;
-  cudaEvent_t t0, t1;
-  CF_CUDA(e, cudaEventCreate(&t0));
-  CF_CUDA(e, cudaEventCreate(&t1));
-  std::vector<std::pair<int, float>> res;
-  for (int n = 4; n <= e->sms; n += (n < 16 ? 4 : 8)) {
-    const int ctas = n > e->sms ? e->sms : n;
-    for (int w = 0; w < 2; ++w) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, ctas, s));
-    CF_CUDA(e, cudaEventRecord(t0, s));
-    for (int r = 0; r < 5; ++r) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, ctas, s));
-    CF_CUDA(e, cudaEventRecord(t1, s));
-    CF_CUDA(e, cudaEventSynchronize(t1));
-    float ms = 0.f;
-    cudaEventElapsedTime(&ms, t0, t1);
-    res.push_back({ctas, ms / 5});
-    e->launches += 14;
-  }
-  {  // all SMs
-    for (int w = 0; w < 2; ++w) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, e->sms, s));
-    CF_CUDA(e, cudaEventRecord(t0, s));
-    for (int r = 0; r < 5; ++r) CF_CUDA(e, launch_decode(e->pm.tk, e->pm.tv, da, e->sms, s));
-    CF_CUDA(e, cudaEventRecord(t1, s));
-    CF_CUDA(e, cudaEventSynchronize(t1));
-    float ms = 0.f;
-    cudaEventElapsedTime(&ms, t0, t1);
-    res.push_back({e->sms, ms / 5});
-    e->launches += 14;
-  }
-  cudaEventDestroy(t0);
-  cudaEventDestroy(t1);
-  float best = 1e30f;
-  for (auto& r : res) best = r.second < best ? r.second : best;
-  int pick = e->sms - 1;
-  for (auto& r : res)
-    if (best / r.second >= frac) {
-      pick = r.first;
-      break;
-    }
-  if (pick >= e->sms) pick = e->sms - 1;
-  e->decode_sms = pick;
-  e->calib.assign(res.begin(), res.end());
+  const DecodeArgs da = step_decode_args(e, bt, ch.rows, pool);   // Q rows of the last step's decodes
+  int pick = 0;
+  st = measure_decode_share(e, da, static_cast<cudaStream_t>(stream), frac, &pick);
+  if (st != CF_OK) return st;
+  e->auto_sms[bucket_of(bt->n_decode)] = pick;
+  e->last_bucket = bucket_of(bt->n_decode);
   *chosen = pick;
   return CF_OK;
 }

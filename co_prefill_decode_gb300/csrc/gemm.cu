@@ -586,12 +586,9 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
                        int num_sms, cudaStream_t s) {
   using C = GemmCfg<BN>;
   auto k = gemm_kernel<BN, EPI>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = smem_limit_per_device(k, (int)C::SMEM, attr);
+  if (e != cudaSuccess) return e;
   const int cap = p.max_ctas > 0 && p.max_ctas < num_sms ? p.max_ctas : num_sms;
   GemmArgs q = p;
   const GemmSchedule sc = gemm_schedule(p.M, p.N, p.K, EPI, cap, (q.sk_ws && q.sk_flags) ? p.split_mode : 1);

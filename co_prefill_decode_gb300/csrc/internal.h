@@ -5,9 +5,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace cf {
 
 constexpr int kPageSize = 16;
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute belongs to the device that is
+// current when it is set, so a process that launches on several GPUs needs
+// it on each.  `done` holds one bit per device index below 64 (devices
+// above that set it on every launch).
+template <typename Kernel>
+cudaError_t smem_limit_per_device(Kernel kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Launches `kernel` with programmatic stream serialisation: it may be
 // scheduled while the previous kernel of the stream finishes; the kernel

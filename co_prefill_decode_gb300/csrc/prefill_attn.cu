@@ -70,6 +70,30 @@ struct PfCfg {
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
+// Registers per thread after the split: the loader / MMA warpgroup gives up
+// registers it does not need and the two softmax warpgroups take them, so
+// the 128 scores of a row stay in registers.  The kernel is launched with
+// kLaunchRegs per thread (384 x 168 = 64512); the split uses all of them,
+// 128 x 88 + 256 x 208 (each softmax thread keeps its row's 128 scores and
+// 16 packed P words in registers without spilling).
+constexpr int kLaunchRegs = 168, kLoaderRegs = 88, kSoftmaxRegs = 208;
+static_assert(128 * kLoaderRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
+
+CF_DEV float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+template <uint32_t N>
+CF_DEV void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+CF_DEV void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 struct Item {
   int qa, ha, qb, hb;   // query tile and head of tiles A and B (qb = -1: no tile B)
   int k0, k1;           // the key tiles [k0, k1) this item visits
@@ -212,6 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_items = a.item_end[a.n_chunks - 1];
   const int oob_row = a.num_pages * a.Hkv * a.page_size;   // first row past the pool
 
+  // The register split is taken inside each warpgroup's own branch, so the
+  // compiler allocates each branch for its own limit.
+  if (warp >= 4) goto softmax_role;
+  regs_dec<kLoaderRegs>();
   if (warp == 0 || warp == 2) {  // ------------------------------------ producers
     // Warp 0 loads Q and the K tiles, warp 2 the V tiles, so the two streams
     // of small boxes are issued in parallel.  In each, lane 0 waits on the
@@ -289,11 +317,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < NBOX)
           tma_load_2d(smem + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE + my_hd * C::HALF + my_page * 2048,
                       is_v ? &tmV : &tmK, full, my_hd * 64, my_row);
-        if (lane == 0) {
-          if (is_v)
-            last_v[st] = ph;
-          else
-            last_k[st] = ph;
+        if (lane == 0) {   // (unrolled so the arrays stay in registers)
+#pragma unroll
+          for (int i = 0; i < NS; ++i)
+            if (i == st) {
+              if (is_v)
+                last_v[i] = ph;
+              else
+                last_k[i] = ph;
+            }
         }
         pid = pid_next;
       }
@@ -304,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int dummy = 0;
       const WaitCtl w2{&dummy, nullptr, a.wait_ns};
       if (last_q != 0xffffffffu) mbar_wait(q_full, last_q, w2);
+#pragma unroll
       for (int i = 0; i < NS; ++i) {
         if (last_k[i] != 0xffffffffu) mbar_wait(&k_full[i], last_k[i], w2);
         if (last_v[i] != 0xffffffffu) mbar_wait(&v_full[i], last_v[i], w2);
@@ -354,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S of key tile k0 for both query tiles
         if (!mbar_wait(&k_full[kc % NS], (kc / NS) & 1, wc)) { ok = false; break; }
         tc_fence_after();
+#pragma unroll
         for (int x = 0; x < 2; ++x)
           if (e[x] > k0) issue_s(x, kc % NS);
         umma_commit(&k_empty[kc % NS]);
@@ -364,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&v_full[vst], (vc / NS) & 1, wc)) { ok = false; break; }
           const bool more = j + 1 < n;
           bool k_ready = false;
+#pragma unroll
           for (int x = 0; x < 2 && ok; ++x) {
             if (j < e[x]) {   // O_x += P_x(j) V_j
               if (!mbar_wait(&p_full[x], pc[x] & 1, wc)) { ok = false; break; }
@@ -402,7 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, 0, w2);
       }
     }
-  } else if (warp >= 4) {  // ------------------------------------------- softmax
+  }
+  goto done;
+softmax_role:
+  {  // ------------------------------------------------------------------ softmax
+    regs_inc<kSoftmaxRegs>();
     const int x = (warp - 4) >> 2;            // query tile A (0) or B (1) of the item
     const int quarter = warp & 3;             // the TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;        // row of the query tile
@@ -442,11 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mp[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = s[i];
+        for (int i = 0; i < 8; ++i) mp[i] = max3f(s[i], s[i + 8], s[i + 16]);
 #pragma unroll
-        for (int c = 8; c < BKV; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
-        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) *
+        for (int c = 24; c < BKV; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mp[i] = c + 8 + i < BKV ? max3f(mp[i], s[c + i], s[c + 8 + i]) : fmaxf(mp[i], s[c + i]);
+        const float mx = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) *
                          a.scale_log2;
         const bool grow = (m == -INFINITY) ? false : (mx > m + kRescaleThreshold);
         if (m == -INFINITY) m = mx;
@@ -469,23 +509,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        const float sc2 = a.scale_log2;
-        float lp[4] = {0.f, 0.f, 0.f, 0.f};
-        // P as bf16 pairs (low half = even key), stored 64 keys at a time
-        // (the registers are read when the store is issued)
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nmu = make_float2(-mu, -mu);
+        float2 lp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        // P as bf16 pairs (low half = even key), stored 32 keys at a time
+        // (the registers are read when the store is issued).  The scaling
+        // and the row sum run as packed fp32 pairs (one instruction per two
+        // keys).
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(s[64 * h + 2 * i], sc2, -mu));
-            const float p1 = fast_exp2(fmaf(s[64 * h + 2 * i + 1], sc2, -mu));
-            lp[i & 3] += p0 + p1;
-            pk[i] = pack_bf16(p0, p1);
+          for (int i = 0; i < 16; ++i) {
+            const float2 xs = __ffma2_rn(make_float2(s[32 * h + 2 * i], s[32 * h + 2 * i + 1]), sc2, nmu);
+            const float2 p = make_float2(fast_exp2(xs.x), fast_exp2(xs.y));
+            lp[i & 1] = __fadd2_rn(lp[i & 1], p);
+            pk[i] = pack_bf16(p.x, p.y);
           }
-          tmem_st32(ts + 32 * h, reinterpret_cast<const float*>(pk));
+          tmem_st16(ts + 16 * h, pk);
         }
-        l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+        l += (lp[0].x + lp[1].x) + (lp[0].y + lp[1].y);
         // Keys past the end of the request: zero their V rows (the slots may
         // hold anything).  The tile whose PV reads V_j first does it: A while
         // it has key tile j, else B.
@@ -566,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+done:
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -639,13 +683,20 @@ __global__ void __launch_bounds__(BQ) prefill_merge_kernel(const __grid_constant
 template <int D>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const PrefillArgs& a,
                      int ctas, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PfCfg<D>::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = smem_limit_per_device(prefill_kernel<D>, (int)PfCfg<D>::SMEM, attr);
+  if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until the registers it asks for are free in the
+  // CTA's launch allocation: refuse to launch a build whose allocation per
+  // thread is below what the split assumes (it would wait forever).
+  static std::atomic<int> regs{0};
+  if (regs.load(std::memory_order_acquire) == 0) {
+    cudaFuncAttributes fa{};
+    const cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+    if (r != cudaSuccess) return r;
+    regs.store(fa.numRegs, std::memory_order_release);
   }
+  if (regs.load(std::memory_order_acquire) < kLaunchRegs) return cudaErrorInvalidConfiguration;
   ctas = prefill_grid(a, ctas);
   if (a.pdl) return launch_pdl(prefill_kernel<D>, dim3(ctas), dim3(kThreads), PfCfg<D>::SMEM, s, q, k, v, a);
   prefill_kernel<D><<<ctas, kThreads, PfCfg<D>::SMEM, s>>>(q, k, v, a);

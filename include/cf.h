@@ -70,7 +70,9 @@ typedef struct {
     int qk_norm;         /* 1: per-head RMSNorm of q and k over d before RoPE    */
     int max_tokens;      /* largest T = l + n_decode of any step                 */
     int max_decode;      /* largest n_decode of any step (<= 2048)               */
-    int decode_sms;      /* SMs given to decode attention in the fork; 0 = auto  */
+    int decode_sms;      /* SMs given to decode attention in the fork; 0 = auto:
+                            the ConfluxServe §6.1 rule, measured per decode-batch
+                            bucket (see cf_calibrate_decode_sms)                 */
 } cf_config;
 
 /* Weights, nn.Linear layout [out_features][in_features], bf16, device. */
@@ -183,6 +185,21 @@ cf_status cf_set_prefill_pairing(cf_engine* e, int mode);
  * use at most 512 partial tiles per launch.  Cut rows agree with uncut ones
  * within fp32 rounding. */
 cf_status cf_set_prefill_split(cf_engine* e, int mode);
+
+/* How cf_layer_step runs decode and prefill attention:
+ *   0 (default) concurrently, on disjoint SM partitions, each side's SMs
+ *     taking over the other side's remaining work items once their own are
+ *     done (ConfluxServe §6.1, "Coordinated attention overlap");
+ *   1 serially, decode alone on all SMs and then prefill alone on all SMs,
+ *     on the caller's stream, with the same kernels and work items: the
+ *     serialized execution that §8.3 (Fig. 14a) measures the overlap
+ *     against.  Its per-phase times (cf_get_phase_times) give each path's
+ *     isolated time ("decode": decode kernel and merge; "prefill": prefill
+ *     kernel and merge), whose larger one is the contention-free bound.
+ * Outputs are the same bits in both modes: the work items, and the order in
+ * which the partials of a cut item are combined, depend neither on the mode
+ * nor on the SM share. */
+cf_status cf_set_fork_mode(cf_engine* e, int mode);
 
 /* Failure-detection self-test (no counterpart on the pages): launches one
  * 128 x 256 GEMM tile on the engine's own buffers whose MMA-issuing thread
@@ -335,14 +352,23 @@ cf_status cf_set_split_k(cf_engine* e, int split_mode);
  * - The first call on each device looks up that array's device address
  *   (with that device current); make that first call before any stream
  *   capture.
+ * - The keys are cut into chunks planned for the num_sms CTAs the call
+ *   launches (0 = all SMs).  With all SMs the output is bit-identical to
+ *   cf_decode_attn's; with fewer it differs from it only in fp32 rounding.
  * - Batches whose scratch would exceed 16 MiB are rejected with
- *   CF_ERR_INVALID_ARG (the need grows with n * Hkv and with the number of
- *   CTAs; a smaller num_sms lowers it).
- * - All calls share the one array, which keeps the last call's contents
- *   (nothing in it has to start at zero): calls that may overlap on the GPU,
- *   e.g. on two streams, race and must be serialised by the caller.
- * - Device-side problems (a page id outside the pool) are skipped as in
- *   cf_decode_attn but are not reported, since there is no engine error word.
+ *   CF_ERR_INVALID_ARG.  The need grows with n * Hkv * G * d and with the
+ *   CTAs launched, so a batch rejected on all SMs may fit with a smaller
+ *   num_sms (e.g. 32 Qwen3-32B-shaped requests need about 22 MB on 152 SMs,
+ *   but fit on up to 116).
+ * - All calls share the one array, which keeps the last call's contents.
+ *   Each call first clears the words that must start at zero (the work-queue
+ *   counter, the error word) on its own stream, so it does not depend on how
+ *   an earlier call ended; calls that may overlap on the GPU, e.g. on two
+ *   streams, race on the array and must be serialised by the caller.
+ * - Device-side problems are not reported, since there is no engine error
+ *   word: a page id outside the pool is skipped (its keys read as zeros) as
+ *   in cf_decode_attn, and a bounded wait that expires ends the kernel with
+ *   part of the output unwritten.  Either way the call returns CF_OK.
  * It calls no cudaMalloc, cudaFree or allocating library routine. */
 cf_status cf_decode_attn_noalloc(int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                                  const void* q, long long q_row_stride, const cf_kv_pool* pool, int n,
@@ -381,11 +407,23 @@ cf_status cf_set_profiling(cf_engine* e, int on);
 /* The decode SM share by the ConfluxServe §6.1 rule: "the minimum number of
  * SMs needed to sustain 90% of its standalone peak HBM bandwidth".  Times the
  * decode attention of batch b (on the Q rows the engine's last cf_layer_step
- * produced, over `pool`) alone at increasing CTA counts, picks the smallest
- * count whose time is within 1/frac of the fastest, stores it as the
- * engine's decode share and returns it in *chosen.  Synchronous; overwrites
- * the engine's attention buffer.  cf_calibration_points copies the measured
- * (CTAs, ms) pairs (returns how many there are). */
+ * produced, over `pool`) alone on 8, 16, ... and all SMs, each point the
+ * median of three launches, picks the smallest count whose time is within
+ * 1/frac of the fastest, stores it as the automatic share of b's decode-batch
+ * bucket (ceil(log2 n_decode)) and returns it in *chosen.  Synchronous;
+ * overwrites the engine's attention buffer.  cf_calibration_points copies
+ * the measured (CTAs, ms) pairs (returns how many there are).
+ *
+ * With decode_sms = 0 (config) and no cf_set_decode_sms override, the first
+ * concurrent cf_layer_step of each bucket that has both decodes and prefill
+ * rows runs this measurement itself, with frac = 0.9, on its own batch after
+ * its QKV stage: that one call blocks the host until the measurement is done
+ * (tens of ms) and its phase times include it.  Make it before any stream
+ * capture: a step on a capturing stream skips the measurement and uses the
+ * bucket's share if known, else a third of the SMs.  The fork is
+ * work-conserving (each side's SMs take the other side's remaining items),
+ * so the rule sets where the two partitions start, not what each may use.
+ * cf_engine_decode_sms reports the share of the last step's bucket. */
 cf_status cf_calibrate_decode_sms(cf_engine* e, const cf_batch* b, const cf_kv_pool* pool, float frac,
                                   void* stream, int* chosen);
 int cf_calibration_points(cf_engine* e, int* sms, float* ms, int cap);

@@ -445,11 +445,12 @@ def test_empty_calls_launch_nothing(cf):
 
 def test_layer_step_is_deterministic_and_launch_count(cf):
     S = LayerSetup(wl.reduced(wl.WORKLOADS["q14b"], (100, 9), 50, 10))
+    first = S.step().clone()          # also measures the automatic decode share
     n0 = S.eng.cf_launch_count()
     a = S.step().clone()
     assert S.eng.cf_launch_count() - n0 == 11   # 9 stages + the fork's second decode and prefill grids
     b = S.step()
-    assert torch.equal(a, b)
+    assert torch.equal(a, b) and torch.equal(a, first)
 
 
 def test_bounded_wait_runs_out_and_the_engine_recovers(cf):
@@ -562,3 +563,79 @@ def test_latency_estimator_fits_and_predicts_through_the_library(cf, tmp_path):
         ranks, chunks = OL.one_gpu(*it)
         assert v["pred_ms"] == pytest.approx(OL.t_iter(m, ranks, chunks)["t_iter"], rel=1e-12)
         assert v["meas_ms"] > 0
+
+
+GRAPH_SLICES = [s for s in SLICES if s[0] in ("tiny", "l8b", "tiny-chunks")]
+
+
+@pytest.mark.parametrize("name,w", GRAPH_SLICES, ids=[s[0] for s in GRAPH_SLICES])
+def test_layer_graphs_chained_parity(cf, name, w):
+    """The piecewise-graph step (ConfluxServe §6.1, Fig. 10: the shared linear
+    segments replayed as CUDA graphs, the attention fork launched eagerly)
+    against the oracle: a replayed step's q, appended k/v, attention output,
+    h and out, at the same bounds as the eager step."""
+    S = LayerSetup(w)
+    S.eng.cf_set_graphs(True)
+    S.step()                                  # captures the two segments
+    assert S.eng.cf_graph_captures() == 1
+    chained(S)                                # replays them
+    assert S.eng.cf_graph_captures() == 1
+    S.eng.cf_set_graphs(False)
+
+
+FORK_SLICES = [s for s in SLICES if s[0] in ("tiny", "l8b", "q14b", "l8b-chunks")]
+
+
+@pytest.mark.parametrize("name,w", FORK_SLICES, ids=[s[0] for s in FORK_SLICES])
+def test_serial_attention_gives_the_fork_bits(cf, name, w):
+    """The serialized execution the fork is measured against (ConfluxServe
+    §8.3, Fig. 14a: decode alone on all SMs, then prefill alone on all SMs)
+    runs the same work items, so it gives the concurrent fork's bits, and it
+    matches the oracle."""
+    S = LayerSetup(w)
+    k0, v0 = S.kp.clone(), S.vp.clone()
+    fork = S.step().clone()
+    attn = S.eng.buffer("attn", S.T).clone()
+    S.kp.copy_(k0)
+    S.vp.copy_(v0)
+    S.eng.cf_set_fork_mode(1)
+    n0 = S.eng.cf_launch_count()
+    serial = S.step().clone()
+    assert torch.equal(serial, fork)
+    assert torch.equal(S.eng.buffer("attn", S.T), attn)
+    assert S.eng.cf_launch_count() - n0 <= 11
+    S.kp.copy_(k0)
+    S.vp.copy_(v0)
+    chained(S)
+    S.eng.cf_set_fork_mode(0)
+    with pytest.raises(cf.CfError):
+        S.eng.cf_set_fork_mode(2)
+
+
+def test_automatic_decode_share_is_the_90_percent_rule(cf):
+    """With decode_sms = 0 the library measures ConfluxServe §6.1's rule on the
+    first step of a decode-batch bucket: the fewest SMs (8, 16, ...) whose
+    decode time is within 1/0.9 of the fastest.  A plain layer step reports
+    that share, not the fallback third of the SMs, and keeps it for later
+    steps of the bucket."""
+    w = wl.reduced(wl.WORKLOADS["l8b"], (4096,) * 16, 256, 0)
+    S = LayerSetup(w)
+    sms = cf.device_sm_count()
+    S.step()
+    pts = S.eng.cf_calibration_points()
+    assert len(pts) >= 2 and pts[-1][0] == sms and all(p[0] % 8 == 0 for p in pts[:-1])
+    best = min(t for _, t in pts)
+    want = next(n for n, t in pts if best / t >= 0.9)
+    want = min(want, sms - 1)
+    got = S.eng.cf_engine_decode_sms()
+    assert got == want
+    assert got % 8 == 0 or got == sms - 1     # a measured point, not the fallback sms / 3
+    n0 = S.eng.cf_launch_count()
+    S.step()
+    assert S.eng.cf_launch_count() - n0 == 11      # measured once per bucket
+    assert S.eng.cf_engine_decode_sms() == got
+    # an explicit share overrides it; 0 returns to the measured one
+    S.eng.cf_set_decode_sms(24)
+    assert S.eng.cf_engine_decode_sms() == 24
+    S.eng.cf_set_decode_sms(0)
+    assert S.eng.cf_engine_decode_sms() == got
