@@ -129,7 +129,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "cf_gemm_schedule": (I, [I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I),
                                  ctypes.POINTER(I)]),
         "cf_set_split_k": (I, [P, I]),
-        "cf_prefill_plan": (I, [I, P, P, I, I, I, I, I, ctypes.POINTER(I), P, ctypes.POINTER(I)]),
+        "cf_prefill_plan": (I, [I, P, P, I, I, I, I, I, ctypes.POINTER(I), P, P, ctypes.POINTER(I)]),
         "cf_decode_plan": (I, [I, P, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(L)]),
         "cf_selftest_timeout": (I, [P, ctypes.c_ulonglong, P]),
         "cf_set_prefill_pairing": (I, [P, I]),
@@ -201,11 +201,13 @@ def cf_prefill_plan(chunks, n_q_heads: int, n_kv_heads: int, sms: int = 152, spl
     lens = (ctypes.c_int * max(n, 1))(*[int(c[0]) for c in chunks])
     prefixes = (ctypes.c_int * max(n, 1))(*[int(c[1]) for c in chunks])
     splits = (ctypes.c_int * max(n, 1))()
+    cut = (ctypes.c_int * max(n, 1))()
     kind, items = ctypes.c_int(), ctypes.c_int()
     _check(lib, None, lib.cf_prefill_plan(n, ctypes.cast(lens, ctypes.c_void_p), ctypes.cast(prefixes, ctypes.c_void_p),
                                           n_q_heads, n_kv_heads, sms, split_mode, pairing_mode, ctypes.byref(kind),
-                                          ctypes.cast(splits, ctypes.c_void_p), ctypes.byref(items)))
-    return {"kind": kind.value, "splits": list(splits)[:n], "items": items.value}
+                                          ctypes.cast(splits, ctypes.c_void_p), ctypes.cast(cut, ctypes.c_void_p),
+                                          ctypes.byref(items)))
+    return {"kind": kind.value, "splits": list(splits)[:n], "cut_from": list(cut)[:n], "items": items.value}
 
 
 def cf_decode_plan(n_keys, page_stride: int, n_kv_heads: int, plan_ctas: int = 152) -> dict:

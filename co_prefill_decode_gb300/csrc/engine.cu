@@ -1170,7 +1170,7 @@ cf_status cf_decode_plan(int n, const int* n_keys, int page_stride, int n_kv_hea
 }
 
 cf_status cf_prefill_plan(int n, const int* len, const int* prefix, int n_q_heads, int n_kv_heads, int sms,
-                          int split_mode, int pairing_mode, int* kind, int* splits, int* items) {
+                          int split_mode, int pairing_mode, int* kind, int* splits, int* cut_from, int* items) {
   if (n <= 0 || n > kMaxChunks || !len || !prefix || n_q_heads <= 0 || n_kv_heads <= 0 || sms <= 0 ||
       n_q_heads % n_kv_heads || split_mode < 0 || split_mode > kPfMaxSplits || pairing_mode < 0 || pairing_mode > 3)
     return CF_ERR_INVALID_ARG;
@@ -1190,7 +1190,10 @@ cf_status cf_prefill_plan(int n, const int* len, const int* prefix, int n_q_head
   prefill_set_chunks(pf, n, len, prefix, row0, off, sms, split_mode);
   for (int s = 0; s < n; ++s)   // slots are sorted by reach: map them back to the given order
     for (int i = 0; i < n; ++i)
-      if (row0[i] == pf.row0[s] && splits) splits[i] = pf.splits[s];
+      if (row0[i] == pf.row0[s]) {
+        if (splits) splits[i] = pf.splits[s];
+        if (cut_from) cut_from[i] = pf.cut_from[s];
+      }
   if (kind) *kind = pf.pair;
   if (items) *items = prefill_items(pf);
   return CF_OK;

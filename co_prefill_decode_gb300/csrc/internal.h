@@ -223,8 +223,9 @@ constexpr int kPfPartTiles = 2048;  // fp32 partial (query tile) slots of split 
 struct PrefillArgs {
   // Work items are numbered chunk slot by chunk slot (slots sorted so that the
   // chunk reaching furthest into its request comes first); slot s owns items
-  // [item_end[s-1], item_end[s]).  A slot's units (tile or tile pair) are cut
-  // into splits[s] key ranges each (1: not cut); item = unit * splits + split.
+  // [item_end[s-1], item_end[s]).  A slot's units (tile or tile pair) before
+  // cut_from[s] are one item each; the later ones are cut into splits[s] key
+  // ranges each, item = cut_from + (unit - cut_from) * splits + split.
   int n_chunks;
   int item_end[kMaxChunks];
   int row0[kMaxChunks];           // the chunk's first row of Q and of out
@@ -232,6 +233,8 @@ struct PrefillArgs {
   int prefix[kMaxChunks];         // c_i
   int page_off[kMaxChunks];       // its page table: pages + page_off, ceil((c_i + l_i) / ps) ids
   int splits[kMaxChunks];
+  int cut_from[kMaxChunks];       // the slot's units before this one run whole; later ones are cut into splits
+  int band[kMaxChunks];           // query tiles per band of the slot's unit order (see unit_tiles)
   int part_base[kMaxChunks];      // first partial slot of the slot's split items (2 per item: A, B)
   int merge_end[kMaxChunks];      // merge blocks of slots 0..s (2 per unit of a cut slot)
   float* part_o;                  // [kPfPartTiles][D][128] unnormalised O of a split's query tile

@@ -56,11 +56,13 @@ template <int D>
 struct PfCfg {
   static constexpr uint32_t HALF = BQ * 64 * 2;          // 16 KB: 128 rows x 64 bf16
   static constexpr uint32_t TILE = HALF * (D / 64);      // one Q, K or V tile
-  static constexpr int KV_STAGES = 2;
+  // K ring one stage deeper than V: the next S needs the next K tile as soon
+  // as the current PV is issued, while V(j) is needed a softmax later
+  static constexpr int K_STAGES = 3, V_STAGES = 2;
   static constexpr uint32_t OFF_Q = 0;                   // Q_A, Q_B
   static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
-  static constexpr uint32_t OFF_V = OFF_K + KV_STAGES * TILE;
-  static constexpr uint32_t OFF_BAR = OFF_V + KV_STAGES * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + V_STAGES * TILE;
   // no alignment slack: the kernel checks that the base is 1 KB aligned
   static constexpr size_t SMEM = OFF_BAR + 512;          // mbarriers, item ring, TMEM address
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -105,20 +107,45 @@ struct Item {
 __host__ __device__ inline int units_of(int kind, int n_qt, int Hq) {
   return kind == kPfHeadPairs ? n_qt * (Hq / 2) : (kind == kPfTilePairs ? (n_qt + 1) / 2 : n_qt) * Hq;
 }
-// Unit u of a chunk with n_qt query tiles, heaviest (last) query tiles
-// first, heads fastest (heads of one KV head adjacent).
-CF_DEV void unit_tiles(int kind, int u, int n_qt, int Hq, Item& it) {
+// Unit u of a chunk with n_qt query tiles.  The query tiles are cut into
+// bands of `band` tiles, the band with the most keys first; within a band
+// the units are numbered KV head by KV head (query tiles with the most keys
+// first, query heads fastest).  CTAs running at the same time then read the
+// K/V of one or two KV heads (about 17 MB each for a 32K-token request at
+// d = 128), which stay in L2, rather than every KV head of the request at
+// scattered key positions.  The band is chosen per chunk so that its query
+// tiles differ by at most about a quarter in key count (16 tiles on a long
+// prefix, 1 without one), so the heaviest units still start first.
+constexpr int kBandQ = 16;
+constexpr int kTailSplits = 4, kTailMinTiles = 8;
+// the KV-head-major position of unit u among n_g groups of c units per KV
+// head (bands of b groups): *r = group index counted from the heaviest,
+// *kvh, *j = index within the (group, KV head)
+CF_DEV void band_order(int u, int n_g, int c, int Hkv, int b, int* r, int* kvh, int* j) {
+  const int band = u / (b * c * Hkv);
+  const int rem = u - band * b * c * Hkv;
+  const int bt = min(b, n_g - band * b);    // groups in this band
+  *kvh = rem / (bt * c);
+  const int rem2 = rem % (bt * c);
+  *r = band * b + rem2 / c;
+  *j = rem2 % c;
+}
+CF_DEV void unit_tiles(int kind, int u, int n_qt, int Hq, int Hkv, int band, Item& it) {
+  const int G = Hq / Hkv;
+  int r, kvh, j;
   if (kind == kPfHeadPairs) {
-    const int hp = Hq / 2;
-    it.qa = it.qb = n_qt - 1 - u / hp;
-    it.ha = 2 * (u % hp);
+    band_order(u, n_qt, G / 2, Hkv, band, &r, &kvh, &j);
+    it.qa = it.qb = n_qt - 1 - r;
+    it.ha = kvh * G + 2 * j;
     it.hb = it.ha + 1;
   } else {
-    const int n_groups = kind == kPfTilePairs ? (n_qt + 1) / 2 : n_qt;
-    const int g = n_groups - 1 - u / Hq;
-    it.ha = it.hb = u % Hq;
-    it.qa = kind == kPfTilePairs ? 2 * g : g;
-    it.qb = (kind == kPfTilePairs && 2 * g + 1 < n_qt) ? 2 * g + 1 : -1;
+    const bool tp = kind == kPfTilePairs;
+    const int n_groups = tp ? (n_qt + 1) / 2 : n_qt;
+    band_order(u, n_groups, G, Hkv, tp ? (band + 1) / 2 : band, &r, &kvh, &j);
+    const int g = n_groups - 1 - r;
+    it.ha = it.hb = kvh * G + j;
+    it.qa = tp ? 2 * g : g;
+    it.qb = (tp && 2 * g + 1 < n_qt) ? 2 * g + 1 : -1;
   }
 }
 CF_DEV int kv_tiles(const Item& it, int qt) {
@@ -137,21 +164,24 @@ CF_DEV void chunk_of(const PrefillArgs& a, int sl, Item& it) {
   it.pages = a.pages + a.page_off[sl];
 }
 
-// Item idx: its chunk slot, its unit and its key range.  Split s of S covers
-// key tiles [s r / S, (s+1) r / S) of the unit's reach r (the key tiles of
-// its later query tile).
+// Item idx: its chunk slot, its unit and its key range.  The slot's units
+// before cut_from run whole, one item each; every later unit is cut into S
+// items, split s covering key tiles [s r / S, (s+1) r / S) of the unit's
+// reach r (the key tiles of its later query tile).
 CF_DEV Item item_at(const PrefillArgs& a, int idx) {
   const int sl = slot_of(a, idx);
   const int local = idx - (sl ? a.item_end[sl - 1] : 0);
   Item it;
   chunk_of(a, sl, it);
-  const int S = a.splits[sl];
-  const int u = local / S, sp = local % S;
-  unit_tiles(a.pair, u, (it.len + BQ - 1) / BQ, a.Hq, it);
+  const int c0 = a.cut_from[sl];
+  const int S = local < c0 ? 1 : a.splits[sl];
+  const int rel = local - c0;   // index among the cut items
+  const int u = local < c0 ? local : c0 + rel / S, sp = local < c0 ? 0 : rel % S;
+  unit_tiles(a.pair, u, (it.len + BQ - 1) / BQ, a.Hq, a.Hkv, a.band[sl], it);
   const int reach = kv_tiles(it, it.qb > it.qa ? it.qb : it.qa);
   it.k0 = sp * reach / S;
   it.k1 = (sp + 1) * reach / S;
-  it.part = S > 1 ? a.part_base[sl] + 2 * local : -1;
+  it.part = S > 1 ? a.part_base[sl] + 2 * rel : -1;
   return it;
 }
 
@@ -160,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
   using C = PfCfg<D>;
-  constexpr int NS = C::KV_STAGES;
+  constexpr int KS = C::K_STAGES, VS = C::V_STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if (smem_u32(smem_raw) & 1023u) {   // the swizzled tiles need a 1 KB aligned base
@@ -170,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;             // [NS]
-  uint64_t* k_empty = k_full + NS;         // [NS]
-  uint64_t* v_full = k_empty + NS;         // [NS]
-  uint64_t* v_empty = v_full + NS;         // [NS]
-  uint64_t* s_full = v_empty + NS;         // [2] per query tile: S ready
+  uint64_t* k_full = bars + 2;             // [KS]
+  uint64_t* k_empty = k_full + KS;         // [KS]
+  uint64_t* v_full = k_empty + KS;         // [VS]
+  uint64_t* v_empty = v_full + VS;         // [VS]
+  uint64_t* s_full = v_empty + VS;         // [2] per query tile: S ready
   uint64_t* p_full = s_full + 2;           // [2] P written
   uint64_t* o_done = p_full + 2;           // [2] the item's last PV is done
   uint64_t* o_free = o_done + 2;           // [2] O read by the epilogue
@@ -200,9 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < KS; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < VS; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
@@ -250,8 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NBOX = 8 * (D / 64);
     int qc = 0, kc = 0;
     bool ok = true;
-    uint32_t last_q = 0xffffffffu, last_k[NS], last_v[NS];
-    for (int i = 0; i < NS; ++i) last_k[i] = last_v[i] = 0xffffffffu;
+    const int NS = is_v ? VS : KS;   // this warp's ring
+    uint32_t last_q = 0xffffffffu, last_k[KS], last_v[VS];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) last_k[i] = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < VS; ++i) last_v[i] = 0xffffffffu;
     for (int k = 0; ok; ++k) {
       // Warp 0 takes the next item once both Q buffers are free and
       // publishes it through an 8-slot ring (no role is more than two items
@@ -318,14 +354,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(smem + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE + my_hd * C::HALF + my_page * 2048,
                       is_v ? &tmV : &tmK, full, my_hd * 64, my_row);
         if (lane == 0) {   // (unrolled so the arrays stay in registers)
+          if (is_v) {
 #pragma unroll
-          for (int i = 0; i < NS; ++i)
-            if (i == st) {
-              if (is_v)
-                last_v[i] = ph;
-              else
-                last_k[i] = ph;
-            }
+            for (int i = 0; i < VS; ++i)
+              if (i == st) last_v[i] = ph;
+          } else {
+#pragma unroll
+            for (int i = 0; i < KS; ++i)
+              if (i == st) last_k[i] = ph;
+          }
         }
         pid = pid_next;
       }
@@ -337,10 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WaitCtl w2{&dummy, nullptr, a.wait_ns};
       if (last_q != 0xffffffffu) mbar_wait(q_full, last_q, w2);
 #pragma unroll
-      for (int i = 0; i < NS; ++i) {
+      for (int i = 0; i < KS; ++i)
         if (last_k[i] != 0xffffffffu) mbar_wait(&k_full[i], last_k[i], w2);
+#pragma unroll
+      for (int i = 0; i < VS; ++i)
         if (last_v[i] != 0xffffffffu) mbar_wait(&v_full[i], last_v[i], w2);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ------------------------------------------------ MMA issuer
@@ -385,17 +423,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(q_full, qc & 1, wc)) { ok = false; break; }
         ++qc;
         // S of key tile k0 for both query tiles
-        if (!mbar_wait(&k_full[kc % NS], (kc / NS) & 1, wc)) { ok = false; break; }
+        if (!mbar_wait(&k_full[kc % KS], (kc / KS) & 1, wc)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x)
-          if (e[x] > k0) issue_s(x, kc % NS);
-        umma_commit(&k_empty[kc % NS]);
+          if (e[x] > k0) issue_s(x, kc % KS);
+        umma_commit(&k_empty[kc % KS]);
         ++kc;
         if (n - k0 == 1) umma_commit(q_empty);
         for (int j = k0; j < n && ok; ++j) {
-          const int vst = vc % NS;
-          if (!mbar_wait(&v_full[vst], (vc / NS) & 1, wc)) { ok = false; break; }
+          const int vst = vc % VS;
+          if (!mbar_wait(&v_full[vst], (vc / VS) & 1, wc)) { ok = false; break; }
           const bool more = j + 1 < n;
           bool k_ready = false;
 #pragma unroll
@@ -413,18 +451,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (more && j + 1 < e[x]) {   // S_x(j+1): overwrites P_x(j) after the PV above has read it
               if (!k_ready) {
-                if (!mbar_wait(&k_full[kc % NS], (kc / NS) & 1, wc)) { ok = false; break; }
+                if (!mbar_wait(&k_full[kc % KS], (kc / KS) & 1, wc)) { ok = false; break; }
                 tc_fence_after();
                 k_ready = true;
               }
-              issue_s(x, kc % NS);
+              issue_s(x, kc % KS);
             }
           }
           if (!ok) break;
           umma_commit(&v_empty[vst]);
           ++vc;
           if (more) {
-            umma_commit(&k_empty[kc % NS]);
+            umma_commit(&k_empty[kc % KS]);
             ++kc;
             if (j + 2 == n) umma_commit(q_empty);   // the item's last S has been issued
           }
@@ -534,8 +572,8 @@ softmax_role:
         // it has key tile j, else B.
         const int vcnt = vbase + (j - it.k0);
         if (kend - kv0 < BKV && (x == 0 || j >= ea)) {
-          const int vst = vcnt % NS;
-          if (!mbar_wait(&v_full[vst], (vcnt / NS) & 1, wc)) ok = false;
+          const int vst = vcnt % VS;
+          if (!mbar_wait(&v_full[vst], (vcnt / VS) & 1, wc)) ok = false;
           const int vk = max(0, kend - kv0);
           uint8_t* vt = smem + C::OFF_V + vst * C::TILE;
           const int nz = (BKV - vk) * (D / 64) * 8;   // 16-byte chunks
@@ -631,16 +669,16 @@ __global__ void __launch_bounds__(BQ) prefill_merge_kernel(const __grid_constant
   int sl = 0;
   while (sl + 1 < a.n_chunks && a.merge_end[sl] <= b) ++sl;
   const int local = b - (sl ? a.merge_end[sl - 1] : 0);
-  const int u = local >> 1, x = local & 1;
+  const int u = a.cut_from[sl] + (local >> 1), x = local & 1;
   Item it;
   chunk_of(a, sl, it);
-  unit_tiles(a.pair, u, (it.len + BQ - 1) / BQ, a.Hq, it);
+  unit_tiles(a.pair, u, (it.len + BQ - 1) / BQ, a.Hq, a.Hkv, a.band[sl], it);
   const int qt = x ? it.qb : it.qa;
   if (qt < 0) return;
   const int qi = qt * BQ + r;
   if (qi >= it.len) return;
   const int S = a.splits[sl];
-  const int P0 = a.part_base[sl] + 2 * u * S + x;   // split s at P0 + 2 s
+  const int P0 = a.part_base[sl] + 2 * (u - a.cut_from[sl]) * S + x;   // split s at P0 + 2 s
   const float2* mlp = reinterpret_cast<const float2*>(a.part_ml) + (size_t)P0 * BQ + r;
   float2 ml[kPfMaxSplits];
   float M = -INFINITY;
@@ -758,7 +796,8 @@ void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix
   for (int i = 0; i < n; ++i) all_units += units[i];
   const int quant = all_units > 0 && all_units < 4 * sms ? std::min(4, (4 * sms + all_units - 1) / all_units) : 1;
   a.n_chunks = n;
-  int items = 0, parts = 0, merges = 0;
+  int split[kMaxChunks], cut[kMaxChunks];
+  bool any_cut = false;
   for (int s = 0; s < n; ++s) {
     const int i = order[s];
     int S = 1;
@@ -769,17 +808,49 @@ void prefill_set_chunks(PrefillArgs& a, int n, const int* len, const int* prefix
       S = std::max(S, std::min(quant, reach_min[i] / 16));
     }
     S = std::min(S, std::min(reach_min[i], kPfMaxSplits));   // every split has a key tile
-    if (S > 1 && parts + 2 * units[i] * S > kPfPartTiles) S = (kPfPartTiles - parts) / (2 * units[i]);
+    split[s] = S < 2 ? 1 : S;
+    cut[s] = 0;
+    any_cut = any_cut || split[s] > 1;
+  }
+  // The tail of a long queue of whole units: when the queue runs dry, SMs
+  // stop up to one unit's time apart (a unit of a Qwen3-32B-shaped chunk on
+  // a 28K prefix runs ~400 us).  So when nothing else is cut and the units
+  // make several waves, the last wave's worth of units (sms, counted from
+  // the end of the queue) is cut into kTailSplits key ranges of at least
+  // kTailMinTiles key tiles: the SMs that reach the tail first take more of
+  // its short items, and the last ones finish close together.
+  if (split_mode == 0 && !any_cut && all_units > 2 * sms) {
+    int tail = sms;
+    for (int s = n - 1; s >= 0 && tail > 0; --s) {
+      const int i = order[s];
+      const int S = std::min(kTailSplits, reach_min[i] / kTailMinTiles);
+      if (S < 2) break;
+      const int take = std::min(units[i], tail);
+      split[s] = S;
+      cut[s] = units[i] - take;
+      tail -= take;
+    }
+  }
+  int items = 0, parts = 0, merges = 0;
+  for (int s = 0; s < n; ++s) {
+    const int i = order[s];
+    int S = split[s];
+    const int n_cut = units[i] - cut[s];
+    if (S > 1 && parts + 2 * n_cut * S > kPfPartTiles) S = (kPfPartTiles - parts) / (2 * n_cut);
     if (S < 2) S = 1;
     a.splits[s] = S;
+    a.cut_from[s] = S > 1 ? cut[s] : units[i];
     a.part_base[s] = S > 1 ? parts : -1;
     if (S > 1) {
-      parts += 2 * units[i] * S;
-      merges += 2 * units[i];
+      parts += 2 * n_cut * S;
+      merges += 2 * n_cut;
     }
-    items += units[i] * S;
+    items += S > 1 ? cut[s] + n_cut * S : units[i];
     a.item_end[s] = items;
     a.merge_end[s] = merges;
+    // query tiles per band of the unit order: tiles whose key counts differ
+    // by at most about a quarter (all 16 on a long prefix, 1 without one)
+    a.band[s] = std::max(1, std::min(kBandQ, (prefix[i] / BQ + 1) / 4));
     a.row0[s] = row0[i];
     a.len[s] = len[i];
     a.prefix[s] = prefix[i];

@@ -153,13 +153,15 @@ cf_status cf_decode_plan(int n, const int* n_keys, int page_stride, int n_kv_hea
  * 0 single 128-row query tiles, 1 pairs of consecutive query tiles of one
  * head, 2 pairs of query heads of one KV head on one query tile (used when
  * Hq / Hkv is even); pairing_mode 0 chooses it as the engine does, 1..3 force
- * kind 0..2.  splits[i]: the key ranges each unit of chunk i is cut into
- * (1: not cut; see cf_set_prefill_split for split_mode); *items: the queue
- * length, sum_i units_i * splits[i].  Any output may be NULL.  Returns
- * CF_ERR_INVALID_ARG for bad sizes, CF_ERR_UNSUPPORTED for head pairs with
- * an odd group. */
+ * kind 0..2.  splits[i]: the key ranges each cut unit of chunk i is cut into
+ * (1: none cut; see cf_set_prefill_split for split_mode); cut_from[i]: the
+ * chunk's units in queue order before this index run whole, the rest are cut
+ * (units_i when none is, 0 when all are); *items: the queue length,
+ * sum_i cut_from[i] + (units_i - cut_from[i]) * splits[i].  Any output may be
+ * NULL.  Returns CF_ERR_INVALID_ARG for bad sizes, CF_ERR_UNSUPPORTED for head
+ * pairs with an odd group. */
 cf_status cf_prefill_plan(int n, const int* len, const int* prefix, int n_q_heads, int n_kv_heads, int sms,
-                          int split_mode, int pairing_mode, int* kind, int* splits, int* items);
+                          int split_mode, int pairing_mode, int* kind, int* splits, int* cut_from, int* items);
 
 /* Work items of prefill attention.  Each item runs two 128-row query tiles
  * that share every K/V tile it loads, or one:
@@ -179,10 +181,14 @@ cf_status cf_set_prefill_pairing(cf_engine* e, int mode);
  * engine workspace; a merge kernel combines the ranges in order, so results
  * are deterministic.  0 (default): cut a chunk's items into
  * ceil(reach / w) ranges when its longest item reaches more than 1.25 w key
- * tiles, w the launch's average key tiles per SM (at least 8); 1 never; n in
- * 2..16 cut every chunk into n ranges where possible.  A chunk is cut into
- * at most as many ranges as its shortest item has key tiles, and cut items
- * use at most 512 partial tiles per launch.  Cut rows agree with uncut ones
+ * tiles, w the launch's average key tiles per SM (at least 8), or into up to
+ * 4 when the launch has fewer than 4 units per SM; when neither applies and
+ * the units make more than two waves, cut the last wave's worth of units of
+ * the queue (one per SM) into 4 ranges of at least 8 key tiles, so that the
+ * SMs finish close together; 1 never; n in 2..16 cut every chunk into n
+ * ranges where possible.  A chunk is cut into at most as many ranges as its
+ * shortest item has key tiles, and cut items use at most 2048 partial query
+ * tiles per launch (128 MB at d = 128).  Cut rows agree with uncut ones
  * within fp32 rounding. */
 cf_status cf_set_prefill_split(cf_engine* e, int mode);
 

@@ -7,7 +7,8 @@ import random
 
 import pytest
 
-BQ = 128          # query tile rows and key tile columns
+BQ = 128          # query tile rows
+BKV = 128         # key tile columns
 MAX_SPLITS = 16
 PART_TILES = 2048
 
@@ -24,7 +25,7 @@ def cf():
 def kv_tiles(prefix, length, qt):
     """Key tiles the query tile qt of a chunk reaches (causal, within the request)."""
     end = min(prefix + (qt + 1) * BQ, prefix + length)
-    return -(-end // BQ)
+    return -(-end // BKV)
 
 
 def units(kind, n_qt, hq):
@@ -40,15 +41,22 @@ def reach_min(kind, prefix, length):
 def test_plans_of_the_layer_workloads(cf):
     p = cf.cf_prefill_plan([(2048, 16384)], 40, 8)
     # odd group: tile pairs; 320 units are fewer than 4 per SM of 152, so each is cut into 2
-    assert p == {"kind": 1, "splits": [2], "items": 640}
+    assert p == {"kind": 1, "splits": [2], "cut_from": [0], "items": 640}
     p = cf.cf_prefill_plan([(4096, 28672)], 64, 8)
-    assert p == {"kind": 2, "splits": [1], "items": 1024}   # 32 tiles x 32 head pairs: enough units
+    # 32 tiles x 32 head pairs = 1024 whole units, more than two waves: the
+    # last wave's worth (152 units) is cut into 4 key ranges
+    assert p == {"kind": 2, "splits": [4], "cut_from": [1024 - 152], "items": 872 + 152 * 4}
     p = cf.cf_prefill_plan([(1024, 0)], 32, 8)
-    assert p == {"kind": 2, "splits": [1], "items": 128}    # the first tile has one key tile: no cut
+    # the first tile has one key tile: no cut
+    assert p == {"kind": 2, "splits": [1], "cut_from": [128], "items": 128}
     # four chunks: units cut where each range keeps >= 16 key tiles
     p = cf.cf_prefill_plan([(1024, 0), (512, 4096), (256, 12288), (128, 2048)], 32, 8)
     assert p["kind"] == 2 and p["splits"] == [1, 2, 3, 1]
+    assert p["cut_from"] == [128, 0, 0, 16]
     assert p["items"] == 16 * (8 * 1 + 4 * 2 + 2 * 3 + 1 * 1)
+    # a long chunk without prefix ends on its lightest units: no tail cut
+    p = cf.cf_prefill_plan([(8192, 0)], 32, 8)
+    assert p == {"kind": 2, "splits": [1], "cut_from": [1024], "items": 1024}
 
 
 def test_forced_modes(cf):
@@ -79,17 +87,24 @@ def test_random_chunk_lists_cover_every_unit(cf, seed):
     assert kind in (0, 1, 2) and (kind != 2 or (hq // hkv) % 2 == 0)
     if (hq // hkv) % 2 == 0:
         assert kind == 2
-    total, parts = 0, 0
-    for (length, prefix), s in zip(chunks, splits):
+    total, parts, tail_cut = 0, 0, False
+    for (length, prefix), s, c in zip(chunks, splits, p["cut_from"]):
         n_qt = -(-length // BQ)
         u = units(kind, n_qt, hq)
         # every range of a cut unit keeps at least one key tile
         assert 1 <= s <= min(MAX_SPLITS, reach_min(kind, prefix, length))
+        assert 0 <= c <= u and (s > 1 or c == u)
         if mode == 1:
             assert s == 1
         if mode >= 2:
-            assert s <= mode
-        total += u * s
-        parts += 2 * u * s if s > 1 else 0
+            assert s <= mode and (s == 1 or c == 0)
+        if s > 1 and c > 0:   # only the tail of a long queue is cut part-way
+            assert mode == 0 and s <= 4 and 8 * s <= reach_min(kind, prefix, length)
+            tail_cut = True
+        total += c + (u - c) * s
+        parts += 2 * (u - c) * s if s > 1 else 0
     assert p["items"] == total
     assert parts <= PART_TILES
+    if tail_cut:   # at most one wave's worth of units is cut at the tail
+        assert sum(u - c for (l, pf), c, s in zip(chunks, p["cut_from"], splits) if s > 1 for u in
+                   [units(kind, -(-l // BQ), hq)]) <= sms
