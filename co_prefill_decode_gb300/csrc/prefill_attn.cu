@@ -499,23 +499,23 @@ softmax_role:
       const int qi = qt * BQ + r;               // query row within the chunk
       const int qpos = it.prefix + qi;
       const int kend = it.prefix + it.len;      // first key that does not exist
-      const int diag = it.prefix + qt * BQ;     // smallest query position of the tile
       float m = -INFINITY, l = 0.f;
       for (int j = it.k0; j < ex; ++j) {
         if (!mbar_wait(&s_full[x], sc & 1, wc)) { ok = false; break; }
         ++sc;
         tc_fence_after();
+        const int kv0 = j * BKV;
+        // this row's visible keys in the tile are a prefix [0, lim): causal
+        // (key <= query position) and within the request
+        const int lim = min(qpos + 1, kend) - kv0;
+        const bool masked = lim < BKV;
         float s[BKV];
 #pragma unroll
         for (int c = 0; c < BKV / 32; ++c) tmem_ld32(ts + c * 32, s + c * 32);
         tmem_ld_wait();
-        const int kv0 = j * BKV;
-        if (kv0 + BKV - 1 > diag) {             // tile crosses the diagonal or the end of the request
+        if (masked) {
 #pragma unroll
-          for (int c = 0; c < BKV; ++c) {
-            const int kp = kv0 + c;
-            if (!(kp <= qpos && kp < kend)) s[c] = -INFINITY;
-          }
+          for (int c = 0; c < BKV; ++c) s[c] = c < lim ? s[c] : -INFINITY;
         }
         float mp[8];
 #pragma unroll
@@ -550,16 +550,26 @@ softmax_role:
         const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
         const float2 nmu = make_float2(-mu, -mu);
         float2 lp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        // P as bf16 pairs (low half = even key), stored 32 keys at a time
-        // (the registers are read when the store is issued).  The scaling
-        // and the row sum run as packed fp32 pairs (one instruction per two
-        // keys).
+        // P as bf16 pairs (low half = even key), from a second pass over S in
+        // TMEM, 32 keys at a time in a loop that is not unrolled: a quarter
+        // of the code of an unrolled pass, which keeps the hot loops of the
+        // warps sharing each scheduler in its instruction cache.  P of chunk
+        // h lands on columns [16 h, 16 h + 16), whose scores an earlier chunk
+        // (or this one) has already read.  Scaling and row sums run as packed
+        // fp32 pairs (one instruction per two keys).
+#pragma unroll 1
+        for (int h = 0; h < BKV / 32; ++h) {
+          float sh[32];
+          tmem_ld32(ts + 32 * h, sh);
+          tmem_ld_wait();
+          if (masked) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+            for (int c = 0; c < 32; ++c) sh[c] = 32 * h + c < lim ? sh[c] : -INFINITY;
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float2 xs = __ffma2_rn(make_float2(s[32 * h + 2 * i], s[32 * h + 2 * i + 1]), sc2, nmu);
+            const float2 xs = __ffma2_rn(make_float2(sh[2 * i], sh[2 * i + 1]), sc2, nmu);
             const float2 p = make_float2(fast_exp2(xs.x), fast_exp2(xs.y));
             lp[i & 1] = __fadd2_rn(lp[i & 1], p);
             pk[i] = pack_bf16(p.x, p.y);
