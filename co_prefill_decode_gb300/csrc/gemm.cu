@@ -34,14 +34,18 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
 
-template <int BN>
+template <int BN, int EPI>
 struct GemmCfg {
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  // per epilogue warp: one 32 x 32 fp32 block being transposed (the SwiGLU
+  // epilogue stores directly and needs none)
+  static constexpr uint32_t XPOSE_BYTES = EPI == EPI_SWIGLU ? 0 : 4 * 32 * 32 * 4;
+  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + XPOSE_BYTES + 256;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 CF_DEV uint8_t* align1024(uint8_t* p) {
@@ -219,10 +223,72 @@ CF_DEV void store_bf16x32(__nv_bfloat16* dst, const float* v) {
   }
 }
 
+// The epilogue reads TMEM one row per thread, so a warp holds a 32-row x
+// 32-column block with each row in one thread.  Stored as it is, every
+// 16-byte store of the warp would touch 32 rows; the block is therefore
+// turned around in shared memory so that each store instruction writes whole
+// 64- or 128-byte row segments.  16-byte chunks are placed XOR-swizzled by
+// the row, which keeps both directions free of bank conflicts.
+//
+// fp32 block (32 words per row): lane l puts row l; afterwards lane l takes
+// row 4i + l/8, columns 4(l%8)..+3, for i = 0..7.
+CF_DEV void xpose_f32_put(float4* sb, const float* v, int lane) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    sb[lane * 8 + (k ^ (lane & 7))] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+CF_DEV float4 xpose_f32_get(const float4* sb, int i, int lane) {
+  const int row = 4 * i + (lane >> 3), k = lane & 7;
+  return sb[row * 8 + (k ^ (row & 7))];
+}
+// bf16 block (16 words per row): lane l puts row l; afterwards lane l takes
+// row 8i + l/4, columns 8(l%4)..+7, for i = 0..3.
+CF_DEV void xpose_b16_put(uint4* sb, const uint32_t* w, int lane) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    sb[lane * 4 + (k ^ ((lane >> 1) & 3))] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+CF_DEV uint4 xpose_b16_get(const uint4* sb, int i, int lane) {
+  const int row = 8 * i + (lane >> 2), k = lane & 3;
+  return sb[row * 4 + (k ^ ((row >> 1) & 3))];
+}
+// 32 fp32 values as 16 words of bf16 pairs (low half = even column)
+CF_DEV void pack32(const float* v, uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+}
+// stores the warp's bf16 block: row r of the block goes to dst0 + r * ld
+CF_DEV void store_block_b16(const uint4* sb, __nv_bfloat16* dst0, size_t ld, int rows_left, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = 8 * i + (lane >> 2);
+    const uint4 q = xpose_b16_get(sb, i, lane);
+    if (row < rows_left) *reinterpret_cast<uint4*>(dst0 + (size_t)row * ld + 8 * (lane & 3)) = q;
+  }
+}
+
+// Stores a warp's 32 rows x 32 columns as bf16 through the transpose: the
+// row held by lane r goes to lane r's `dst` (nothing where it is null).
+CF_DEV void store_rows_b16(uint4* sb, __nv_bfloat16* dst, const float* v, int lane) {
+  uint32_t pk[16];
+  pack32(v, pk);
+  __syncwarp();
+  xpose_b16_put(sb, pk, lane);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = 8 * i + (lane >> 2);
+    __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), row));
+    const uint4 q = xpose_b16_get(sb, i, lane);
+    if (d) *reinterpret_cast<uint4*>(d + 8 * (lane & 3)) = q;
+  }
+}
+
 // QKV epilogue for one head of one row: columns [hcol, hcol + D) of this
 // thread's TMEM lane hold q, k or v of head `head` for stacked row `row`.
 template <int D>
-CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpilogue& e) {
+CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpilogue& e, uint4* sb, int lane) {
   const int Hq = e.Hq, Hkv = e.Hkv;
   const int kind = head < Hq ? 0 : (head < Hq + Hkv ? 1 : 2);
   __nv_bfloat16* dst = nullptr;
@@ -245,7 +311,7 @@ CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpi
     for (int c = 0; c < D / 32; ++c) {
       tmem_ld32(taddr + c * 32, v);
       tmem_ld_wait();
-      if (dst) store_bf16x32(dst + c * 32, v);
+      store_rows_b16(sb, dst ? dst + c * 32 : nullptr, v, lane);
     }
     return;
   }
@@ -270,7 +336,6 @@ CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpi
     tmem_ld32(taddr + c * 32, v);
     tmem_ld32(taddr + D / 2 + c * 32, w);
     tmem_ld_wait();
-    if (!dst) continue;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int i0 = c * 32 + i;
@@ -283,8 +348,8 @@ CF_DEV void qkv_head(uint32_t taddr, int row, bool valid, int head, const QkvEpi
       v[i] = x1 * r.x - x2 * r.y;
       w[i] = x1 * r.y + x2 * r.x;
     }
-    store_bf16x32(dst + c * 32, v);
-    store_bf16x32(dst + D / 2 + c * 32, w);
+    store_rows_b16(sb, dst ? dst + c * 32 : nullptr, v, lane);
+    store_rows_b16(sb, dst ? dst + D / 2 + c * 32 : nullptr, w, lane);
   }
 }
 
@@ -292,11 +357,12 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, GemmArgs p) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, EPI>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint8_t* xpose = smem + STAGES * C::STAGE_BYTES;   // 4 KB per epilogue warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(xpose + C::XPOSE_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -459,6 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r_in_tile = quarter * 32 + lane;
     const int ep_tid = threadIdx.x - 64;
+    float4* xf32 = reinterpret_cast<float4*>(xpose + quarter * 4096);
+    uint4* xb16 = reinterpret_cast<uint4*>(xpose + quarter * 4096);
     griddep_wait();   // the epilogue reads the residual / RoPE table and writes
     int it = 0;
     UnitIter ui(blockIdx.x, gridDim.x, num_kb, p.tiles, p.dp_tiles, p.split);
@@ -483,69 +551,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       float v[32], w[32];
+      uint32_t pk[16];
+      // this warp's 32 rows of the tile start at tile row quarter * 32
+      const int wrow0 = mt * BM + quarter * 32;
+      const int rows_left = p.M - wrow0;
       if constexpr (EPI == EPI_BF16) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * BN;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)wrow0 * p.ldo + nt * BN;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           tmem_ld32(taddr + c, v);
           tmem_ld_wait();
-          if (valid) store_bf16x32(out + c, v);
+          pack32(v, pk);
+          __syncwarp();
+          xpose_b16_put(xb16, pk, lane);
+          __syncwarp();
+          store_block_b16(xb16, out + c, p.ldo, rows_left, lane);
         }
       } else if constexpr (EPI == EPI_RESID_F32) {
-        // the residual of chunk c + 32 is loaded while chunk c is read from
-        // TMEM and stored, so only the first chunk waits for its loads
-        float* out = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + nt * BN;
-        const uint4* res = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.aux) +
-                                                          (size_t)row * p.ld_aux + nt * BN);
-        uint4 rn[4];
+        // out (fp32) = acc + residual (bf16); lane l handles rows 4i + l/8,
+        // columns 4(l%8)..+3 of each 32-column block, and the residual of the
+        // next block is loaded while this one is turned around and stored
+        float* out = reinterpret_cast<float*>(p.out) + (size_t)wrow0 * p.ldo + nt * BN + 4 * (lane & 7);
+        const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(p.aux) + (size_t)wrow0 * p.ld_aux +
+                                   nt * BN + 4 * (lane & 7);
+        uint2 rn[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) rn[i] = valid ? res[i] : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 8; ++i) {
+          const int row = 4 * i + (lane >> 3);
+          rn[i] = row < rows_left ? *reinterpret_cast<const uint2*>(res + (size_t)row * p.ld_aux) : make_uint2(0, 0);
+        }
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          uint4 rc[4];
+          uint2 rc[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) rc[i] = rn[i];
-          if (valid && c + 32 < BN) {
+          for (int i = 0; i < 8; ++i) rc[i] = rn[i];
+          if (c + 32 < BN) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) rn[i] = res[(c + 32) / 8 + i];
+            for (int i = 0; i < 8; ++i) {
+              const int row = 4 * i + (lane >> 3);
+              if (row < rows_left) rn[i] = *reinterpret_cast<const uint2*>(res + (size_t)row * p.ld_aux + c + 32);
+            }
           }
           tmem_ld32(taddr + c, v);
           tmem_ld_wait();
-          if (valid) {
-            float4* o4 = reinterpret_cast<float4*>(out + c);
+          __syncwarp();
+          xpose_f32_put(xf32, v, lane);
+          __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 q = rc[i];
-              o4[2 * i] = make_float4(v[8 * i + 0] + bf16lo(q.x), v[8 * i + 1] + bf16hi(q.x),
-                                      v[8 * i + 2] + bf16lo(q.y), v[8 * i + 3] + bf16hi(q.y));
-              o4[2 * i + 1] = make_float4(v[8 * i + 4] + bf16lo(q.z), v[8 * i + 5] + bf16hi(q.z),
-                                          v[8 * i + 6] + bf16lo(q.w), v[8 * i + 7] + bf16hi(q.w));
-            }
+          for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + (lane >> 3);
+            const float4 a = xpose_f32_get(xf32, i, lane);
+            if (row < rows_left)
+              *reinterpret_cast<float4*>(out + (size_t)row * p.ldo + c) =
+                  make_float4(a.x + bf16lo(rc[i].x), a.y + bf16hi(rc[i].x), a.z + bf16lo(rc[i].y), a.w + bf16hi(rc[i].y));
           }
         }
       } else if constexpr (EPI == EPI_RESID_BF16) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * BN;
-        const float* res = reinterpret_cast<const float*>(p.aux) + (size_t)row * p.ld_aux + nt * BN;
+        // out (bf16) = bf16(acc + residual (fp32)), same lane layout as above
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)wrow0 * p.ldo + nt * BN + 4 * (lane & 7);
+        const float* res = reinterpret_cast<const float*>(p.aux) + (size_t)wrow0 * p.ld_aux + nt * BN + 4 * (lane & 7);
+        float4 rn[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = 4 * i + (lane >> 3);
+          rn[i] = row < rows_left ? *reinterpret_cast<const float4*>(res + (size_t)row * p.ld_aux) : make_float4(0, 0, 0, 0);
+        }
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          tmem_ld32(taddr + c, v);
-          tmem_ld_wait();
-          if (valid) {
-            const float4* r4 = reinterpret_cast<const float4*>(res + c);
+          float4 rc[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rc[i] = rn[i];
+          if (c + 32 < BN) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float4 q = r4[i];
-              v[4 * i] += q.x;
-              v[4 * i + 1] += q.y;
-              v[4 * i + 2] += q.z;
-              v[4 * i + 3] += q.w;
+              const int row = 4 * i + (lane >> 3);
+              if (row < rows_left) rn[i] = *reinterpret_cast<const float4*>(res + (size_t)row * p.ld_aux + c + 32);
             }
-            store_bf16x32(out + c, v);
+          }
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          __syncwarp();
+          xpose_f32_put(xf32, v, lane);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + (lane >> 3);
+            const float4 a = xpose_f32_get(xf32, i, lane);
+            if (row < rows_left)
+              *reinterpret_cast<uint2*>(out + (size_t)row * p.ldo + c) =
+                  make_uint2(pack_bf16(a.x + rc[i].x, a.y + rc[i].y), pack_bf16(a.z + rc[i].z, a.w + rc[i].w));
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
-        __nv_bfloat16* out =
-            reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * (BN / 2);
+        // stored directly, one row per thread: measured faster here than
+        // through the transpose (the SiLU work already spaces the stores)
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * (BN / 2);
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           tmem_ld32(taddr + c, v);
@@ -563,11 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (D == 128) {
 #pragma unroll 1
           for (int hh = 0; hh < BN / 128; ++hh)
-            qkv_head<128>(taddr + hh * 128, row, valid, (col0 + hh * 128) / 128, p.qkv);
+            qkv_head<128>(taddr + hh * 128, row, valid, (col0 + hh * 128) / 128, p.qkv, xb16, lane);
         } else {
 #pragma unroll 1
           for (int hh = 0; hh < BN / 64; ++hh)
-            qkv_head<64>(taddr + hh * 64, row, valid, (col0 + hh * 64) / 64, p.qkv);
+            qkv_head<64>(taddr + hh * 64, row, valid, (col0 + hh * 64) / 64, p.qkv, xb16, lane);
         }
       }
       tc_fence_before();
@@ -584,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int EPI>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const GemmArgs& p,
                        int num_sms, cudaStream_t s) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, EPI>;
   auto k = gemm_kernel<BN, EPI>;
   static std::atomic<unsigned long long> attr{0};
   const cudaError_t e = smem_limit_per_device(k, (int)C::SMEM, attr);
