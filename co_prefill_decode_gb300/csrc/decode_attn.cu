@@ -14,16 +14,20 @@
 // (V), which the swizzle makes bank-conflict free.
 //
 // The two small contractions per page, S = Q_g K^T (G x 16 keys) and
-// O += P V (G x d), run on mma.sync m16n8k16 with the G query heads as the
-// M rows: with only part of the SMs, G = 4..8 rows of CUDA-core FMAs per
-// key would not keep up with the HBM stream.  For G <= 8 the otherwise
-// padded rows 8..15 of the P V product carry the low bf16 half of P
-// (P = hi + lo), so P V is accurate to ~2^-16 at no extra MMA cost.
+// O += P V (G x d), run on mma.sync m16n8k16: with only part of the SMs,
+// G = 4..8 rows of CUDA-core FMAs per key would not keep up with the HBM
+// stream.  For G <= 8 they are computed transposed (S^T = K Q^T, O^T += V^T
+// P^T), with the page's 16 keys as the M rows and the heads as N = 8: half
+// the MMAs of the heads-as-rows form, whose S products were half padding.
+// For 8 < G <= 16 the heads are the M rows, and P is split into bf16 high
+// and low parts (P = hi + lo) so that P V keeps ~2^-16 of P's precision.
 //
 // Partial results (unnormalised O, running max m in log2 units, sum l) of
 // the chunks of one (request, head) are merged with the log-sum-exp rule
 // (Decode Token Parallelism §4.4, Eq. 4: partial outputs with fp32
 // log-sum-exp statistics): o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -220,6 +224,98 @@ CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, co
   }
 }
 
+// ---- G <= 8: the products transposed, so the 16 keys of a page are the
+// MMA's M rows and the query heads its N columns:
+//   S^T = K Q^T   (m16n8k16: 16 keys x 8 heads, d in steps of 16),
+//   O^T += V^T P^T (16 values of d x 8 heads per MMA, the page's 16 keys as K).
+// A page then costs D/16 + D/16 MMAs instead of 2 D/8 with the heads as rows,
+// where half of every S product was padding.  P is rounded to bf16 as the B
+// operand; each head's running max moves only when one of its scores passes
+// it by more than 2^8, which a warp vote detects without a reduction.
+template <int D>
+struct AccT {
+  float o[D / 16][4];   // O^T: d = 16 m + g ([0], [1]) and 16 m + g + 8 ([2], [3]); heads 2t (+0), 2t+1 (+1)
+  float m[2];           // running max (log2 units) of heads 2t and 2t + 1
+  float l[2];           // their sums over the keys this lane holds
+};
+
+CF_DEV uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <int D>
+CF_DEV void process_page_t(AccT<D>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
+                           float scale_log2, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  // ---- S^T = K Q^T; K rows are the A operand, the Q fragments (head g,
+  // d = 16 s + 2t (+8)) are exactly the B operand's; two accumulator chains
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int st = 0; st < D / 16; ++st) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(kt + swz((lane & 7) + 8 * ((lane >> 3) & 1), 2 * st + (lane >> 4)), a0, a1, a2, a3);
+    mma16816(st & 1 ? c1 : c0, a0, a1, a2, a3, qa[st][0], qa[st][1]);
+  }
+  // x[k][e]: key g + 8 k, head 2t + e, in log2 units; keys past the end are -inf
+  float x[2][2];
+  x[0][0] = g < valid ? (c0[0] + c1[0]) * scale_log2 : -INFINITY;
+  x[0][1] = g < valid ? (c0[1] + c1[1]) * scale_log2 : -INFINITY;
+  x[1][0] = g + 8 < valid ? (c0[2] + c1[2]) * scale_log2 : -INFINITY;
+  x[1][1] = g + 8 < valid ? (c0[3] + c1[3]) * scale_log2 : -INFINITY;
+  bool need = false;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) need |= fmaxf(x[0][e], x[1][e]) > A.m[e] + kRescaleThreshold;   // -inf + 8 = -inf
+  if (__any_sync(0xffffffffu, need)) {
+    // the page's max per head: keys g, g + 8 here, g over the lanes 4 g + t
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float mx = fmaxf(x[0][e], x[1][e]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      if (mx > A.m[e] + kRescaleThreshold) {   // the same for the 8 lanes of this head
+        const float alpha = fast_exp2(A.m[e] - mx);   // 0 when the head had no keys yet
+        A.l[e] *= alpha;
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+          A.o[m][e] *= alpha;
+          A.o[m][2 + e] *= alpha;
+        }
+        A.m[e] = mx;
+      }
+    }
+  }
+  float p[2][2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const float mu = A.m[e] == -INFINITY ? 0.f : A.m[e];
+    p[0][e] = fast_exp2(x[0][e] - mu);
+    p[1][e] = fast_exp2(x[1][e] - mu);
+    A.l[e] += p[0][e] + p[1][e];
+  }
+  // P^T as this lane holds it (key g or g + 8; heads 2t, 2t + 1) is one row
+  // of an 8x8 block; the B operand wants keys 2t, 2t + 1 of head g: the
+  // transpose of that block
+  const uint32_t b0 = movmatrix_trans(pack_bf16(p[0][0], p[0][1]));
+  const uint32_t b1 = movmatrix_trans(pack_bf16(p[1][0], p[1][1]));
+  // keys past the end of the request: their V (any bits, even NaN) must not
+  // reach the product, so zero those halves of the A fragments
+  uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+  if (valid < 16) {
+    vm0 = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+    vm1 = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
+  }
+  // ---- O^T += V^T P^T: V read transposed (rows of d, the page's keys as K)
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(vt + swz((lane & 7) + 8 * (lane >> 4), 2 * m + ((lane >> 3) & 1)), a0, a1, a2, a3);
+    mma16816(A.o[m], a0 & vm0, a1 & vm0, a2 & vm1, a3 & vm1, b0, b1);
+  }
+}
+
 // Writes one query head's row: either the normalised bf16 output or the
 // fp32 partial (unnormalised O plus m, l).  Lane (g, t) holds d = 8m + 2t, +1.
 template <int D>
@@ -241,6 +337,105 @@ CF_DEV void write_row(const float (*o)[2], float m, float l, bool final_out, __n
   }
 }
 
+
+// Per item: zero the accumulator, and at the end write the item's rows.
+template <int D, bool G16>
+CF_DEV void acc_init(Acc<D, G16>& A) {
+#pragma unroll
+  for (int m = 0; m < D / 8; ++m) {
+    A.o[m][0] = A.o[m][1] = 0.f;
+    A.o8[m][0] = A.o8[m][1] = 0.f;
+  }
+  A.m0 = A.m1 = -INFINITY;
+  A.l0 = A.l1 = 0.f;
+}
+template <int D>
+CF_DEV void acc_init(AccT<D>& A) {
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) A.o[m][0] = A.o[m][1] = A.o[m][2] = A.o[m][3] = 0.f;
+  A.m[0] = A.m[1] = -INFINITY;
+  A.l[0] = A.l[1] = 0.f;
+}
+template <int D, bool G16>
+CF_DEV void acc_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
+                     const uint32_t (*qb)[2], float scale_log2, int lane) {
+  process_page<D, G16>(A, kt, vt, valid, qa, qb, scale_log2, lane);
+}
+template <int D>
+CF_DEV void acc_page(AccT<D>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
+                     const uint32_t (*)[2], float scale_log2, int lane) {
+  process_page_t<D>(A, kt, vt, valid, qa, scale_log2, lane);
+}
+// rows of query heads h G + i, i < G, of request j: the output (final) or
+// the item's partial at index `slot`
+template <int D, bool G16>
+CF_DEV void acc_finish(Acc<D, G16>& A, const DecodeArgs& a, int j, int h, int G, long long slot, bool final_out,
+                       int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 1);
+  A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 2);
+  if constexpr (G16) {
+    A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 1);
+    A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 2);
+  } else {
+#pragma unroll
+    for (int m = 0; m < D / 8; ++m) {
+      A.o[m][0] += A.o8[m][0];
+      A.o[m][1] += A.o8[m][1];
+    }
+  }
+  if (g < G) {
+    __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + g) * D;
+    float* prow = a.part_o + ((size_t)slot * G + g) * D;
+    float* ml = a.part_ml + ((size_t)slot * G + g) * 2;
+    write_row<D>(A.o, A.m0, A.l0, final_out, orow, prow, ml, t);
+  }
+  if constexpr (G16) {
+    if (g + 8 < G) {
+      __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + g + 8) * D;
+      float* prow = a.part_o + ((size_t)slot * G + g + 8) * D;
+      float* ml = a.part_ml + ((size_t)slot * G + g + 8) * 2;
+      write_row<D>(A.o8, A.m1, A.l1, final_out, orow, prow, ml, t);
+    }
+  }
+}
+template <int D>
+CF_DEV void acc_finish(AccT<D>& A, const DecodeArgs& a, int j, int h, int G, long long slot, bool final_out,
+                       int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {   // a head's keys are spread over the lanes 4 g + t
+    A.l[e] += __shfl_xor_sync(0xffffffffu, A.l[e], 4);
+    A.l[e] += __shfl_xor_sync(0xffffffffu, A.l[e], 8);
+    A.l[e] += __shfl_xor_sync(0xffffffffu, A.l[e], 16);
+  }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int hh = 2 * t + e;
+    if (hh >= G) continue;
+    if (final_out) {
+      const float inv = A.l[e] > 0.f ? 1.0f / A.l[e] : 0.f;
+      __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + hh) * D;
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m) {
+        orow[16 * m + g] = __float2bfloat16(A.o[m][e] * inv);
+        orow[16 * m + g + 8] = __float2bfloat16(A.o[m][2 + e] * inv);
+      }
+    } else {
+      float* prow = a.part_o + ((size_t)slot * G + hh) * D;
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m) {
+        prow[16 * m + g] = A.o[m][e];
+        prow[16 * m + g + 8] = A.o[m][2 + e];
+      }
+      if (g == 0) {
+        float* ml = a.part_ml + ((size_t)slot * G + hh) * 2;
+        ml[0] = A.m[e];
+        ml[1] = A.l[e];
+      }
+    }
+  }
+}
 // Chunking plan, computed identically by every CTA of every grid from the
 // key counts: pages_j = ceil(keys_j / 16); chunk = max(4, ceil(sum_j pages_j
 // * Hkv / (ipw * warps))) with warps = 8 * plan_ctas; chunks_j =
@@ -376,14 +571,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         qb[st][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qrow + (g + 8) * D + 16 * st + 8 + 2 * t) : 0u;
       }
     }
-    Acc<D, G16> A;
-#pragma unroll
-    for (int m = 0; m < D / 8; ++m) {
-      A.o[m][0] = A.o[m][1] = 0.f;
-      A.o8[m][0] = A.o8[m][1] = 0.f;
-    }
-    A.m0 = A.m1 = -INFINITY;
-    A.l0 = A.l1 = 0.f;
+    // G <= 8: the transposed products; G > 8: the query heads as MMA rows
+    typename std::conditional<G16, Acc<D, true>, AccT<D>>::type A;
+    acc_init(A);
 
     // ring pipeline: up to STAGES pages in flight; lane 0 issues the TMA
     // copies of page p0 + k into slot (issued % STAGES)
@@ -422,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         valid = 0;
       }
       const uint32_t kt = ring + sl * R::PAGE;
-      process_page<D, G16>(A, kt, kt + R::KV, valid, qa, qb, a.scale_log2, lane);
+      acc_page(A, kt, kt + R::KV, valid, qa, qb, a.scale_log2, lane);
       ++consumed;
       __syncwarp();   // every lane has read the slot before it is refilled
       if (k_issue < np) {
@@ -446,34 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok_run) break;
-    A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 1);
-    A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 2);
-    if constexpr (G16) {
-      A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 1);
-      A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 2);
-    } else {
-#pragma unroll
-      for (int m = 0; m < D / 8; ++m) {
-        A.o[m][0] += A.o8[m][0];
-        A.o[m][1] += A.o8[m][1];
-      }
-    }
-    const bool final_out = nch == 1;
-    const long long slot = item;  // partial index = (S_j + c) * Hkv + h
-    if (g < G) {
-      __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + g) * D;
-      float* prow = a.part_o + ((size_t)slot * G + g) * D;
-      float* ml = a.part_ml + ((size_t)slot * G + g) * 2;
-      write_row<D>(A.o, A.m0, A.l0, final_out, orow, prow, ml, t);
-    }
-    if constexpr (G16) {
-      if (g + 8 < G) {
-        __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + g + 8) * D;
-        float* prow = a.part_o + ((size_t)slot * G + g + 8) * D;
-        float* ml = a.part_ml + ((size_t)slot * G + g + 8) * 2;
-        write_row<D>(A.o8, A.m1, A.l1, final_out, orow, prow, ml, t);
-      }
-    }
+    acc_finish(A, a, j, h, G, item, nch == 1, lane);   // partial index = (S_j + c) * Hkv + h
     if (lane == 0) item = atomicAdd(a.counter, 1);
     item = __shfl_sync(0xffffffffu, item, 0);
   }
