@@ -194,6 +194,10 @@ DECODE_CASES = [
     ("q14b", wl.QWEN14B, (33, 1000, 15)),
     ("q32b", wl.QWEN32B, (3000, 31, 64)),
     ("g16", wl.LayerShape(2048, 32, 2, 64, 512, 1e4, 1e-5, False), (90, 1, 300)),
+    # group sizes that leave some of the transposed products' 8 head columns unused
+    ("g1", wl.LayerShape(1024, 8, 8, 128, 512, 1e4, 1e-5, False), (40, 1, 130)),
+    ("g3", wl.LayerShape(768, 6, 2, 128, 512, 1e4, 1e-5, False), (77, 16, 500)),
+    ("g7", wl.LayerShape(1792, 14, 2, 128, 512, 1e4, 1e-5, False), (33, 260)),
     # one long request: ~250 chunks, so the merge reads (m, l) beyond the 64 it keeps in registers
     ("long1", wl.LLAMA8B, (20000,)),
 ]
