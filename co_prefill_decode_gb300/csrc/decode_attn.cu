@@ -79,18 +79,20 @@ CF_DEV void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int D, bool G16>
-struct Acc {
-  float o[D / 8][2];      // row g: d = 8 m + 2 t, +1
-  float o8[D / 8][2];     // row g + 8: heads 8..15 (G > 8) or the low part of P (G <= 8)
-  float m0, l0, m1, l1;
+// ---- 8 < G <= 16: the query heads are the MMA's M rows (heads 0..7 in
+// rows g, heads 8..15 in rows g + 8).
+template <int D>
+struct Acc16 {
+  float o[D / 8][2];      // head g: d = 8 m + 2 t, +1
+  float o8[D / 8][2];     // head g + 8
+  float m0, l0, m1, l1;   // running max (log2 units) and sum of heads g and g + 8
 };
 
 // One page (16 keys) of one item: S = Q K^T, online softmax, O += P V.
 // kt, vt: shared-memory addresses of the page's K and V tiles.
-template <int D, bool G16>
-CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
-                         const uint32_t (*qb)[2], float scale_log2, int lane) {
+template <int D>
+CF_DEV void process_page16(Acc16<D>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
+                           const uint32_t (*qb)[2], float scale_log2, int lane) {
   const int t = lane & 3;
   // ---- S = Q K^T: two n-tiles of 8 keys, two accumulator chains each
   float s[2][4];
@@ -106,10 +108,8 @@ CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, co
       for (int n = 0; n < 2; ++n) {
         uint32_t b[4];
         ldsm_x4(kt + swz(8 * n + (lane & 7), 4 * sp + (lane >> 3)), b[0], b[1], b[2], b[3]);
-        mma16816(e0[n], qa[2 * sp][0], G16 ? qb[2 * sp][0] : 0u, qa[2 * sp][1], G16 ? qb[2 * sp][1] : 0u, b[0],
-                 b[1]);
-        mma16816(e1[n], qa[2 * sp + 1][0], G16 ? qb[2 * sp + 1][0] : 0u, qa[2 * sp + 1][1],
-                 G16 ? qb[2 * sp + 1][1] : 0u, b[2], b[3]);
+        mma16816(e0[n], qa[2 * sp][0], qb[2 * sp][0], qa[2 * sp][1], qb[2 * sp][1], b[0], b[1]);
+        mma16816(e1[n], qa[2 * sp + 1][0], qb[2 * sp + 1][0], qa[2 * sp + 1][1], qb[2 * sp + 1][1], b[2], b[3]);
       }
 #pragma unroll
     for (int n = 0; n < 2; ++n)
@@ -130,7 +130,8 @@ CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, co
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   // lazy rescaling: keep the running max unless it grows by more than 2^8
-  // (P then stays below 256, exact enough in fp32 and in the bf16 hi/lo split)
+  // (P then stays below 256, exact enough in fp32 and in the bf16 hi/lo split);
+  // heads g first, then heads g + 8
   const bool first = A.m0 == -INFINITY;
   const bool grow = !first && mx > A.m0 + kRescaleThreshold;
   if (first) A.m0 = mx;
@@ -142,10 +143,6 @@ CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, co
     for (int m = 0; m < D / 8; ++m) {
       A.o[m][0] *= alpha;
       A.o[m][1] *= alpha;
-      if constexpr (!G16) {
-        A.o8[m][0] *= alpha;
-        A.o8[m][1] *= alpha;
-      }
     }
   }
   const float muse = A.m0 == -INFINITY ? 0.f : A.m0;
@@ -160,13 +157,12 @@ CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, co
     }
   A.l0 += ls;
   // P is split into bf16 high and low parts: P ~= hi + lo, hi = bf16(P),
-  // lo = bf16(P - hi).
+  // lo = bf16(P - hi); the low parts go through a second MMA.
   const uint32_t pa0 = pack_bf16(p[0][0], p[0][1]), pa2 = pack_bf16(p[1][0], p[1][1]);
   const uint32_t pl0 = pack_bf16(p[0][0] - bf16lo(pa0), p[0][1] - bf16hi(pa0));
   const uint32_t pl2 = pack_bf16(p[1][0] - bf16lo(pa2), p[1][1] - bf16hi(pa2));
-  uint32_t pa1 = pl0, pa3 = pl2;     // G <= 8: rows g+8 of the MMA carry the low part
-  uint32_t ql1 = 0u, ql3 = 0u;
-  if constexpr (G16) {
+  uint32_t pa1, pa3, ql1, ql3;
+  {
     float my = fmaxf(fmaxf(y[0][0], y[0][1]), fmaxf(y[1][0], y[1][1]));
     my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
     my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
@@ -215,7 +211,7 @@ CF_DEV void process_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, co
       const uint32_t b0 = b[2 * u] & vm0, b1 = b[2 * u + 1] & vm1;
       float c[4] = {A.o[m + u][0], A.o[m + u][1], A.o8[m + u][0], A.o8[m + u][1]};
       mma16816(c, pa0, pa1, pa2, pa3, b0, b1);
-      if constexpr (G16) mma16816(c, pl0, ql1, pl2, ql3, b0, b1);   // low parts of both row groups
+      mma16816(c, pl0, ql1, pl2, ql3, b0, b1);   // low parts of both row groups
       A.o[m + u][0] = c[0];
       A.o[m + u][1] = c[1];
       A.o8[m + u][0] = c[2];
@@ -339,8 +335,8 @@ CF_DEV void write_row(const float (*o)[2], float m, float l, bool final_out, __n
 
 
 // Per item: zero the accumulator, and at the end write the item's rows.
-template <int D, bool G16>
-CF_DEV void acc_init(Acc<D, G16>& A) {
+template <int D>
+CF_DEV void acc_init(Acc16<D>& A) {
 #pragma unroll
   for (int m = 0; m < D / 8; ++m) {
     A.o[m][0] = A.o[m][1] = 0.f;
@@ -356,10 +352,10 @@ CF_DEV void acc_init(AccT<D>& A) {
   A.m[0] = A.m[1] = -INFINITY;
   A.l[0] = A.l[1] = 0.f;
 }
-template <int D, bool G16>
-CF_DEV void acc_page(Acc<D, G16>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
+template <int D>
+CF_DEV void acc_page(Acc16<D>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
                      const uint32_t (*qb)[2], float scale_log2, int lane) {
-  process_page<D, G16>(A, kt, vt, valid, qa, qb, scale_log2, lane);
+  process_page16<D>(A, kt, vt, valid, qa, qb, scale_log2, lane);
 }
 template <int D>
 CF_DEV void acc_page(AccT<D>& A, uint32_t kt, uint32_t vt, int valid, const uint32_t (*qa)[2],
@@ -368,35 +364,25 @@ CF_DEV void acc_page(AccT<D>& A, uint32_t kt, uint32_t vt, int valid, const uint
 }
 // rows of query heads h G + i, i < G, of request j: the output (final) or
 // the item's partial at index `slot`
-template <int D, bool G16>
-CF_DEV void acc_finish(Acc<D, G16>& A, const DecodeArgs& a, int j, int h, int G, long long slot, bool final_out,
+template <int D>
+CF_DEV void acc_finish(Acc16<D>& A, const DecodeArgs& a, int j, int h, int G, long long slot, bool final_out,
                        int lane) {
   const int g = lane >> 2, t = lane & 3;
   A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 1);
   A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, 2);
-  if constexpr (G16) {
-    A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 1);
-    A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 2);
-  } else {
-#pragma unroll
-    for (int m = 0; m < D / 8; ++m) {
-      A.o[m][0] += A.o8[m][0];
-      A.o[m][1] += A.o8[m][1];
-    }
-  }
+  A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 1);
+  A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, 2);
   if (g < G) {
     __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + g) * D;
     float* prow = a.part_o + ((size_t)slot * G + g) * D;
     float* ml = a.part_ml + ((size_t)slot * G + g) * 2;
     write_row<D>(A.o, A.m0, A.l0, final_out, orow, prow, ml, t);
   }
-  if constexpr (G16) {
-    if (g + 8 < G) {
-      __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + g + 8) * D;
-      float* prow = a.part_o + ((size_t)slot * G + g + 8) * D;
-      float* ml = a.part_ml + ((size_t)slot * G + g + 8) * 2;
-      write_row<D>(A.o8, A.m1, A.l1, final_out, orow, prow, ml, t);
-    }
+  if (g + 8 < G) {
+    __nv_bfloat16* orow = a.out + (size_t)j * a.out_stride + (size_t)(h * G + g + 8) * D;
+    float* prow = a.part_o + ((size_t)slot * G + g + 8) * D;
+    float* ml = a.part_ml + ((size_t)slot * G + g + 8) * 2;
+    write_row<D>(A.o8, A.m1, A.l1, final_out, orow, prow, ml, t);
   }
 }
 template <int D>
@@ -572,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // G <= 8: the transposed products; G > 8: the query heads as MMA rows
-    typename std::conditional<G16, Acc<D, true>, AccT<D>>::type A;
+    typename std::conditional<G16, Acc16<D>, AccT<D>>::type A;
     acc_init(A);
 
     // ring pipeline: up to STAGES pages in flight; lane 0 issues the TMA
