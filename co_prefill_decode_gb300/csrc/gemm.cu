@@ -5,7 +5,8 @@
 // thread of warp 1 issues tcgen05.mma (M=128, N=BN, K=16, bf16 -> fp32 in
 // TMEM) and commits each stage back to the producer; warps 2-5 read the
 // accumulator from TMEM (double buffered, so the epilogue of tile i overlaps
-// the MMAs of tile i+1) and apply the fused epilogue.  The stacked
+// the MMAs of tile i+1) and apply the fused epilogue, storing whole row
+// segments through a per-warp shared-memory transpose.  The stacked
 // [prefill; decode] token matrix is the A operand, so every weight tile is
 // fetched once for both phases (ConfluxServe §4 "Cross-SP co-batch", App. B
 // Table 7: weight traffic amortised over all co-batched tokens).
