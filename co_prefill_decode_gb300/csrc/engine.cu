@@ -479,7 +479,7 @@ DecodeArgs step_decode_args(cf_engine* e, const cf_batch* bt, int chunk_rows, co
 
 // ConfluxServe §6.1: decode gets "the minimum number of SMs needed to
 // sustain 90% of its standalone peak HBM bandwidth".  Times the decode
-// attention `da` alone (kernel + merge, on `s`) on 8, 16, ..., all SMs,
+// attention `da` alone (kernel + merge, on `s`) on 8, 12, 16, ..., all SMs,
 // each point the median of three timed launches after a warm-up one, and
 // picks the smallest CTA count whose time is within 1/frac of the fastest.
 // Synchronous (waits for the work already queued on `s`); overwrites the
@@ -489,7 +489,7 @@ cf_status measure_decode_share(cf_engine* e, const DecodeArgs& da, cudaStream_t 
   for (auto& x : ev) CF_CUDA(e, cudaEventCreate(&x));
   std::vector<std::pair<int, float>> res;
   cf_status st = CF_OK;
-  for (int n = 8;; n += 8) {
+  for (int n = 8;; n += 4) {   // 4-SM steps: the pick sits close to where the curve crosses the rule
     const int ctas = n < e->sms ? n : e->sms;
     cudaError_t r = launch_decode(e->pm.tk, e->pm.tv, da, ctas, s);
     for (int k = 0; k < 3 && r == cudaSuccess; ++k) {

@@ -413,7 +413,7 @@ cf_status cf_set_profiling(cf_engine* e, int on);
 /* The decode SM share by the ConfluxServe §6.1 rule: "the minimum number of
  * SMs needed to sustain 90% of its standalone peak HBM bandwidth".  Times the
  * decode attention of batch b (on the Q rows the engine's last cf_layer_step
- * produced, over `pool`) alone on 8, 16, ... and all SMs, each point the
+ * produced, over `pool`) alone on 8, 12, 16, ... and all SMs, each point the
  * median of three launches, picks the smallest count whose time is within
  * 1/frac of the fastest, stores it as the automatic share of b's decode-batch
  * bucket (ceil(log2 n_decode)) and returns it in *chosen.  Synchronous;
