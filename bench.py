@@ -38,7 +38,6 @@ METRIC = "co-batched layer step µs & tokens/s; decode attn % HBM peak; GEMM % B
 # in "source"); an entry is removed whenever its kernel changes.
 DOMINANT_TRAFFIC = {
     ("q32b", "prefill"): {"bytes": 351844608 + 93404160, "source": "profiles/prefill_attn_q32b_4096on28672.md"},
-    ("l8b", "gateup"): {"bytes": 243573504 + 21564416, "source": "profiles/gemm_gateup_l8b_T1040.md"},
 }
 
 # The kernels of a step that a roofline can name: phase of the engine's
